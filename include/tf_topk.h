@@ -1,0 +1,123 @@
+/*
+ * tf_topk.h -- exact per-row top-k over wide bf16 logit rows, on GB300 (sm_103a).
+ *
+ * The operation: TensorFold PR #713, "perf(qwen27): a drafted round overlaps
+ * its cache commit with the next draft, and the drafter's attention and top-k
+ * use more of the GPU".
+ *   - Change 3 of the PR's list: each row of a bf16 draft-head logit matrix
+ *     (15 rows x 98592 columns there) yields its best k entries, ordered by
+ *     score descending and, between equal scores, by the lower token index.
+ *     Wide rows are scanned in column spans and the span results merged in the
+ *     same order; a compile-time check ties the kernel constants (lanes, spans,
+ *     max_k) to the host side.
+ *   - The "Exactness" table: each row reports its entries, a count and a
+ *     non-finite mask; the cases cover widths 4096 to 248320, ties, both
+ *     zeros, NaN, infinities and padded row strides, and a "Row ABI and guards"
+ *     check validates the call's arguments.
+ *
+ * Conventions the pages leave open (the same readings as the CPU oracle):
+ *   - a NaN (any sign or payload) is never selected;
+ *   - +0 and -0 are equal scores (they tie, the lower column wins); every
+ *     reported value keeps the original bits of its column;
+ *   - +inf and -inf are ordinary extreme scores; subnormals are exact;
+ *   - count = min(k, number of non-NaN columns of the row);
+ *   - mask = (row has NaN ? 1 : 0) | (has +inf ? 2 : 0) | (has -inf ? 4 : 0),
+ *     over columns [0, cols) only;
+ *   - slots count..k-1 hold index -1 and value bits 0x7FC0.
+ * The result is unique (ties are broken by column), so two correct
+ * implementations agree bit for bit.
+ *
+ * Every call is asynchronous on the given stream and returns after the launch;
+ * device faults, if any, surface at the caller's next synchronisation.  The
+ * library allocates nothing and keeps no per-call state, so calls on any
+ * streams and host threads may overlap.  On an error return nothing has been
+ * launched and no output has been written.
+ */
+#ifndef TF_TOPK_H
+#define TF_TOPK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest k a call accepts (the pages' max_k constant; its value is not given
+ * there -- 64 is the largest k of the workloads this library targets). */
+#define TF_TOPK_MAX_K 64
+/* Most column spans (cooperating CTAs) one row may be split over. */
+#define TF_TOPK_MAX_SPANS 16
+
+/* Status codes. */
+#define TF_TOPK_OK 0
+#define TF_TOPK_ERR_NULL 1   /* a required pointer is NULL (rows > 0) */
+#define TF_TOPK_ERR_SHAPE 2  /* rows < 0, cols < 1, row_stride < cols, cols >= 2^31,
+                                or rows * row_stride overflows */
+#define TF_TOPK_ERR_K 3      /* k < 1 or k > TF_TOPK_MAX_K */
+#define TF_TOPK_ERR_ALIGN 4  /* logits/out_val not 2-byte, out_idx/out_count/mask not
+                                4-byte aligned */
+#define TF_TOPK_ERR_SPANS 5  /* tf_topk_bf16_spans: spans not in {0,1,2,4,8,16} */
+#define TF_TOPK_ERR_DEVICE 6 /* current device is not compute capability 10.3 */
+#define TF_TOPK_ERR_CUDA 7   /* a CUDA runtime call or the launch failed; see
+                                tf_topk_last_cuda_error() */
+
+/*
+ * Exact top-k of every row of a bf16 matrix.
+ *
+ *   logits             device pointer, bf16 bit patterns, row r at
+ *                      logits + r * row_stride (elements); columns
+ *                      [cols, row_stride) are padding and are never read.
+ *                      Any 2-byte-aligned address and any row_stride >= cols
+ *                      are accepted.
+ *   rows, cols         matrix shape; rows == 0 is a no-op returning TF_TOPK_OK.
+ *   row_stride         elements between row starts.
+ *   k                  1..TF_TOPK_MAX_K; k > cols is allowed (empty slots).
+ *   out_idx            device, int32 [rows][k]: selected column indices.
+ *   out_val            device, uint16 [rows][k]: bf16 bits of those columns.
+ *   out_count          device, int32 [rows].
+ *   out_nonfinite_mask device, uint32 [rows].
+ *   stream             cudaStream_t to launch on (NULL = the legacy default
+ *                      stream).
+ * All buffers are owned by the caller; outputs must not overlap the input.
+ * The call runs on the current CUDA device.  Returns a TF_TOPK_* status.
+ */
+int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                 int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                 uint32_t *out_nonfinite_mask, void *stream);
+
+/*
+ * The same operation with the launch plan named by the caller (for cross-path
+ * tests and A/B timing).  spans = 1 runs one CTA per row over the whole row
+ * (the control path, as the pages keep a single-group kernel as the control);
+ * spans in {2, 4, 8, 16} splits each row into that many column spans scanned
+ * by the CTAs of one thread-block cluster and merged through distributed
+ * shared memory; spans = 0 picks the plan tf_topk_bf16 would use.  Results
+ * are identical for every plan.
+ */
+int tf_topk_bf16_spans(const void *logits, int64_t rows, int64_t cols, int64_t row_stride,
+                       int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                       uint32_t *out_nonfinite_mask, int32_t spans, void *stream);
+
+/* The span count tf_topk_bf16 picks for this shape on the current device
+ * (>= 1), or a negative TF_TOPK_* status if the shape is invalid. */
+int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k);
+
+/* Compile-time constants of the kernels, exported so a host-side check can
+ * compare them with the header (the pages' constant tie between kernel and
+ * host). */
+int32_t tf_topk_bf16_max_k(void);         /* == TF_TOPK_MAX_K */
+int32_t tf_topk_bf16_max_spans(void);     /* == TF_TOPK_MAX_SPANS */
+int32_t tf_topk_bf16_cta_threads(void);   /* threads per CTA */
+int32_t tf_topk_bf16_chunk_columns(void); /* columns one CTA holds in registers per pass */
+
+/* Human-readable text for a TF_TOPK_* status (static storage). */
+const char *tf_topk_strerror(int status);
+
+/* cudaError_t value behind the calling thread's last TF_TOPK_ERR_CUDA (0 if none). */
+int tf_topk_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TF_TOPK_H */

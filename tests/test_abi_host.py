@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/tf_topk.h declares, its compile-time constants match
+the header (the kernel/host constant tie of TensorFold PR #713, change 3), and
+the argument guards ("Row ABI and guards" in the PR's "Exactness" table)
+reject bad calls before any CUDA work."""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "tf_topk.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from wide_bf16_row_gb300 import build
+    build.build()
+    from wide_bf16_row_gb300 import topk
+    return topk.library()
+
+
+def declared_functions() -> list[str]:
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tf_topk_\w+)\s*\(", text)))
+
+
+def header_macros() -> dict[str, int]:
+    out = {}
+    for name, val in re.findall(r"#define\s+(TF_TOPK_\w+)\s+(\d+)", HEADER.read_text()):
+        out[name] = int(val)
+    return out
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "tf_topk_bf16" in names and len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in tf_topk.h but not exported"
+    nm = subprocess.run(["nm", "-D", "--defined-only", str(ROOT / "wide_bf16_row_gb300" / "libtf_topk.so")],
+                        capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (tf_topk_\w+)", nm))
+    assert set(names) <= exported
+
+
+def test_constants_match_header(lib):
+    from wide_bf16_row_gb300 import topk
+    macros = header_macros()
+    c = topk.constants()
+    assert c["max_k"] == macros["TF_TOPK_MAX_K"] == topk.MAX_K
+    assert c["max_spans"] == macros["TF_TOPK_MAX_SPANS"]
+    assert c["cta_threads"] % 32 == 0
+    assert c["chunk_columns"] <= 65536 and c["chunk_columns"] % (8 * c["cta_threads"]) == 0
+    for i, name in enumerate(["TF_TOPK_OK", "TF_TOPK_ERR_NULL", "TF_TOPK_ERR_SHAPE", "TF_TOPK_ERR_K",
+                              "TF_TOPK_ERR_ALIGN", "TF_TOPK_ERR_SPANS", "TF_TOPK_ERR_DEVICE",
+                              "TF_TOPK_ERR_CUDA"]):
+        assert macros[name] == i
+        assert getattr(topk, name.replace("TF_TOPK_", "")) == i
+
+
+FAKE = 0x10000  # a non-NULL, aligned address; guards reject before it is touched
+
+
+def call(lib, logits=FAKE, rows=4, cols=100, stride=100, k=8, idx=FAKE, val=FAKE, count=FAKE,
+         mask=FAKE, spans=None):
+    if spans is None:
+        return lib.tf_topk_bf16(logits, rows, cols, stride, k, idx, val, count, mask, None)
+    return lib.tf_topk_bf16_spans(logits, rows, cols, stride, k, idx, val, count, mask, spans, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(k=0), 3), (dict(k=65), 3), (dict(k=-1), 3),
+    (dict(cols=0), 2), (dict(rows=-1), 2), (dict(stride=99), 2), (dict(cols=2**31, stride=2**31), 2),
+    (dict(rows=2**40, stride=2**30, cols=100), 2),
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(val=None), 1), (dict(count=None), 1),
+    (dict(mask=None), 1),
+    (dict(logits=FAKE + 1), 4), (dict(idx=FAKE + 2), 4), (dict(val=FAKE + 1), 4),
+    (dict(count=FAKE + 2), 4), (dict(mask=FAKE + 1), 4),
+    (dict(spans=3), 5), (dict(spans=32), 5), (dict(spans=-1), 5),
+])
+def test_guards_reject_before_launch(lib, kwargs, status):
+    assert call(lib, **kwargs) == status
+
+
+def test_zero_rows_is_a_no_op(lib):
+    assert call(lib, rows=0, logits=None, idx=None, val=None, count=None, mask=None) == 0
+    assert call(lib, rows=0, spans=16) == 0
+
+
+def test_strerror_covers_every_status(lib):
+    from wide_bf16_row_gb300 import topk
+    texts = {topk.strerror(s) for s in range(8)}
+    assert len(texts) == 8 and "unknown status" not in texts
+    assert topk.strerror(99) == "unknown status"
+
+
+def test_product_path_never_touches_the_oracle():
+    """The CUDA library and the binding share no code with the oracle."""
+    pkg = ROOT / "wide_bf16_row_gb300"
+    for p in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.h")):
+        text = p.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, p
+        assert "topk_oracle" not in text, p
+    nm = subprocess.run(["nm", "-D", str(pkg / "libtf_topk.so")], capture_output=True, text=True).stdout
+    assert "oracle" not in nm
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    from wide_bf16_row_gb300 import topk
+    monkeypatch.setattr(topk, "_lib", None)
+    monkeypatch.setattr(topk, "LIBRARY", tmp_path / "missing.so")
+    with pytest.raises(ImportError):
+        topk.library()

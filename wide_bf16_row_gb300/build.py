@@ -1,0 +1,53 @@
+"""Build the CUDA library ``libtf_topk.so`` in-tree for sm_103a.
+
+``python -m wide_bf16_row_gb300.build`` (or ``__graft_entry__.build()``) runs
+nvcc once; the result sits next to this file, where the binding loads it.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+ROOT = PKG.parent
+SOURCES = [PKG / "csrc" / "tf_topk.cu"]
+HEADERS = [ROOT / "include" / "tf_topk.h"]
+LIBRARY = PKG / "libtf_topk.so"
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def nvcc() -> str:
+    cand = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    return cand
+
+
+def command(out: Path) -> list[str]:
+    return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
+            "-I", str(ROOT / "include"), "-o", str(out), *map(str, SOURCES)]
+
+
+def up_to_date() -> bool:
+    if not LIBRARY.exists():
+        return False
+    t = LIBRARY.stat().st_mtime
+    return all(p.stat().st_mtime <= t for p in SOURCES + HEADERS)
+
+
+def build(force: bool = False, verbose: bool = False) -> Path:
+    if up_to_date() and not force:
+        return LIBRARY
+    tmp = LIBRARY.with_name(f"{LIBRARY.name}.tmp{os.getpid()}")
+    cmd = command(tmp)
+    if verbose:
+        print(" ".join(cmd), file=sys.stderr)
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, LIBRARY)
+    return LIBRARY
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)
+    print(LIBRARY)

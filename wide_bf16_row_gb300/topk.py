@@ -1,0 +1,151 @@
+"""Python binding over ``libtf_topk.so`` (C ABI in ``include/tf_topk.h``).
+
+Argument marshalling only: every step of the top-k runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, every entry point raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+PKG = Path(__file__).resolve().parent
+LIBRARY = PKG / "libtf_topk.so"
+
+# status codes (include/tf_topk.h)
+OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_SPANS, ERR_DEVICE, ERR_CUDA = range(8)
+
+_lib = None
+
+
+class TopkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"tf_topk status {status}: {message}")
+        self.status = status
+
+
+def library() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it was never built."""
+    global _lib
+    if _lib is None:
+        if not LIBRARY.exists():
+            raise ImportError(f"{LIBRARY} is missing: build it with "
+                              "`python -m wide_bf16_row_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(str(LIBRARY))
+        c_i64, c_i32, c_p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+        lib.tf_topk_bf16.restype = ctypes.c_int
+        lib.tf_topk_bf16.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
+        lib.tf_topk_bf16_spans.restype = ctypes.c_int
+        lib.tf_topk_bf16_spans.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p,
+                                           c_i32, c_p]
+        lib.tf_topk_bf16_plan.restype = c_i32
+        lib.tf_topk_bf16_plan.argtypes = [c_i64, c_i64, c_i32]
+        for name in ("tf_topk_bf16_max_k", "tf_topk_bf16_max_spans", "tf_topk_bf16_cta_threads",
+                     "tf_topk_bf16_chunk_columns"):
+            getattr(lib, name).restype = c_i32
+            getattr(lib, name).argtypes = []
+        lib.tf_topk_strerror.restype = ctypes.c_char_p
+        lib.tf_topk_strerror.argtypes = [ctypes.c_int]
+        lib.tf_topk_last_cuda_error.restype = ctypes.c_int
+        lib.tf_topk_last_cuda_error.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return library().tf_topk_strerror(status).decode()
+
+
+def constants() -> dict:
+    lib = library()
+    return {
+        "max_k": lib.tf_topk_bf16_max_k(),
+        "max_spans": lib.tf_topk_bf16_max_spans(),
+        "cta_threads": lib.tf_topk_bf16_cta_threads(),
+        "chunk_columns": lib.tf_topk_bf16_chunk_columns(),
+    }
+
+
+MAX_K = 64
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        msg = strerror(status)
+        if status == ERR_CUDA:
+            msg += f" (cudaError {library().tf_topk_last_cuda_error()})"
+        raise TopkError(status, msg)
+
+
+def tf_topk_bf16(logits: int, rows: int, cols: int, row_stride: int, k: int, out_idx: int,
+                 out_val: int, out_count: int, out_nonfinite_mask: int, stream: int | None) -> int:
+    """The C entry point with raw pointers (ints); returns the status code."""
+    return library().tf_topk_bf16(logits, rows, cols, row_stride, k, out_idx, out_val, out_count,
+                                  out_nonfinite_mask, stream)
+
+
+def tf_topk_bf16_spans(logits: int, rows: int, cols: int, row_stride: int, k: int, out_idx: int,
+                       out_val: int, out_count: int, out_nonfinite_mask: int, spans: int,
+                       stream: int | None) -> int:
+    """The C entry point with an explicit span count; returns the status code."""
+    return library().tf_topk_bf16_spans(logits, rows, cols, row_stride, k, out_idx, out_val,
+                                        out_count, out_nonfinite_mask, spans, stream)
+
+
+def plan(rows: int, cols: int, k: int) -> int:
+    """Span count the library picks for a shape on the current device."""
+    r = library().tf_topk_bf16_plan(rows, cols, k)
+    if r < 0:
+        _check(-r)
+    return r
+
+
+def topk_bf16(x, k: int, *, spans: int = 0, out=None, stream=None):
+    """Exact top-k of every row of a CUDA bf16 matrix.
+
+    ``x``: a CUDA tensor of dtype bfloat16 (or int16/uint16 holding bf16 bits),
+    1-D (one row) or 2-D with unit column stride; ``x.stride(0)`` is the row
+    stride, so a column-sliced view of a padded buffer works as is.
+    Returns ``(idx int32[rows,k], val bfloat16[rows,k], count int32[rows],
+    mask int32[rows])``; ``mask`` holds the uint32 bits (1 NaN, 2 +inf, 4 -inf).
+    ``out`` may supply those four tensors.  Runs on ``stream`` (a
+    ``torch.cuda.Stream``) or the current stream of ``x``'s device.
+    """
+    import torch
+
+    if not x.is_cuda:
+        raise ValueError("topk_bf16 needs a CUDA tensor (no CPU path exists)")
+    if x.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"expected bf16 bits, got {x.dtype}")
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dim() != 2:
+        raise ValueError("x must be 1-D or 2-D")
+    rows, cols = x.shape
+    if cols > 1 and x.stride(1) != 1:
+        raise ValueError("columns must be contiguous (stride(1) == 1)")
+    row_stride = x.stride(0) if rows > 1 else max(cols, x.stride(0))
+    dev = x.device
+    if out is None:
+        idx = torch.empty((rows, k), dtype=torch.int32, device=dev)
+        val = torch.empty((rows, k), dtype=torch.bfloat16, device=dev)
+        count = torch.empty((rows,), dtype=torch.int32, device=dev)
+        mask = torch.empty((rows,), dtype=torch.int32, device=dev)
+    else:
+        idx, val, count, mask = out
+        for t, shape, dtypes in ((idx, (rows, k), (torch.int32,)),
+                                 (val, (rows, k), (torch.bfloat16, torch.int16, torch.uint16)),
+                                 (count, (rows,), (torch.int32,)),
+                                 (mask, (rows,), (torch.int32, torch.uint32))):
+            if tuple(t.shape) != shape or t.dtype not in dtypes or not t.is_contiguous() \
+                    or t.device != dev:
+                raise ValueError("out tensors must be contiguous, on x's device, with shapes "
+                                 "(rows,k), (rows,k), (rows,), (rows,)")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        status = tf_topk_bf16_spans(x.data_ptr(), rows, cols, row_stride, k, idx.data_ptr(),
+                                    val.data_ptr(), count.data_ptr(), mask.data_ptr(), spans,
+                                    stream.cuda_stream)
+    _check(status)
+    return idx, val, count, mask
