@@ -1,7 +1,7 @@
 """Benchmark: exact per-row bf16 top-k on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--spans S]
+                    [--workload NAME] [--plan P]
 
 A step is one call of the whole path (load, key encode, span select, span
 merge, write) over one batch: the 256 x 248320 bf16 draft window with k = 20
@@ -284,11 +284,11 @@ def run_ours(args) -> None:
            torch.empty((rows,), dtype=torch.int32, device=dev),
            torch.empty((rows,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
-    spans = args.spans
-    plan = spans if spans else topk.plan(rows, cols, k)
+    plan_arg = args.plan
+    plan = plan_arg if plan_arg else topk.plan(rows, cols, k)
 
     def step(i: int):
-        topk.topk_bf16(views[i % nbuf], k, spans=spans, out=out, stream=stream)
+        topk.topk_bf16(views[i % nbuf], k, plan=plan_arg, out=out, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -345,7 +345,7 @@ def run_ours(args) -> None:
     h_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out)
     for _ in range(2):
         dbuf.copy_(pinned_in, non_blocking=True)
-        topk.topk_bf16(dview, k, spans=spans, out=out, stream=stream)
+        topk.topk_bf16(dview, k, plan=plan_arg, out=out, stream=stream)
         for h, d in zip(h_out, out):
             h.copy_(d, non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -355,7 +355,7 @@ def run_ours(args) -> None:
     e0.record(stream)
     for _ in range(e2e_steps):
         dbuf.copy_(pinned_in, non_blocking=True)
-        topk.topk_bf16(dview, k, spans=spans, out=out, stream=stream)
+        topk.topk_bf16(dview, k, plan=plan_arg, out=out, stream=stream)
         for h, d in zip(h_out, out):
             h.copy_(d, non_blocking=True)
     e1.record(stream)
@@ -384,7 +384,8 @@ def run_ours(args) -> None:
             "dtype": "u16",
             "data": "synthetic",
             "config": workload_config(w, {
-                "spans": plan,
+                "plan": {1: "single", 2: "cluster2", 4: "cluster4", 8: "cluster8", 16: "cluster16",
+                         32: "stream"}.get(plan, str(plan)),
                 "l2": f"inputs rotate over {nbuf} device copies ({nbuf * in_bytes / 1e6:.0f} MB, "
                       f"L2 {l2 / 1e6:.0f} MB)",
                 "parallelism": f"replicas x{world} (rows independent, no exchange)"}),
@@ -413,7 +414,8 @@ def main(argv=None) -> None:
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--spans", type=int, default=0, help="0 = the library's plan")
+    ap.add_argument("--plan", type=int, default=0,
+                    help="TF_TOPK_PLAN_* code: 0 auto, 1 single, 2/4/8/16 cluster, 32 stream")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

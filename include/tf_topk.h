@@ -29,8 +29,9 @@
  *
  * Every call is asynchronous on the given stream and returns after the launch;
  * device faults, if any, surface at the caller's next synchronisation.  The
- * library allocates nothing and keeps no per-call state, so calls on any
- * streams and host threads may overlap.  On an error return nothing has been
+ * library allocates no output and keeps no per-call state beyond its
+ * per-stream scratch, so calls on different streams and host threads may
+ * overlap.  On an error return nothing has been
  * launched and no output has been written.
  */
 #ifndef TF_TOPK_H
@@ -45,7 +46,8 @@ extern "C" {
 /* Largest k a call accepts (the pages' max_k constant; its value is not given
  * there -- 64 is the largest k of the workloads this library targets). */
 #define TF_TOPK_MAX_K 64
-/* Most column spans (cooperating CTAs) one row may be split over. */
+/* Most column spans (cooperating CTAs) one row may be split over, and most
+ * pieces a row is cut into by the stream plan. */
 #define TF_TOPK_MAX_SPANS 16
 
 /* Status codes. */
@@ -56,7 +58,7 @@ extern "C" {
 #define TF_TOPK_ERR_K 3      /* k < 1 or k > TF_TOPK_MAX_K */
 #define TF_TOPK_ERR_ALIGN 4  /* logits/out_val not 2-byte, out_idx/out_count/mask not
                                 4-byte aligned */
-#define TF_TOPK_ERR_SPANS 5  /* tf_topk_bf16_spans: spans not in {0,1,2,4,8,16} */
+#define TF_TOPK_ERR_PLAN 5   /* tf_topk_bf16_with_plan: unknown plan code */
 #define TF_TOPK_ERR_DEVICE 6 /* current device is not compute capability 10.3 */
 #define TF_TOPK_ERR_CUDA 7   /* a CUDA runtime call or the launch failed; see
                                 tf_topk_last_cuda_error() */
@@ -80,27 +82,53 @@ extern "C" {
  *                      stream).
  * All buffers are owned by the caller; outputs must not overlap the input.
  * The call runs on the current CUDA device.  Returns a TF_TOPK_* status.
+ *
+ * Scratch: the default (stream) plan keeps a small per-(device, stream) area
+ * (two k-entry lists and a ticket per CTA, under 1 MB) that the library
+ * allocates on the first call on that stream and keeps until exit.  That first
+ * call therefore allocates (cudaMalloc) and should not be made during stream
+ * capture.  Outputs are never allocated by the library.
  */
 int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
                  int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
                  uint32_t *out_nonfinite_mask, void *stream);
 
-/*
- * The same operation with the launch plan named by the caller (for cross-path
- * tests and A/B timing).  spans = 1 runs one CTA per row over the whole row
- * (the control path, as the pages keep a single-group kernel as the control);
- * spans in {2, 4, 8, 16} splits each row into that many column spans scanned
- * by the CTAs of one thread-block cluster and merged through distributed
- * shared memory; spans = 0 picks the plan tf_topk_bf16 would use.  Results
- * are identical for every plan.
- */
-int tf_topk_bf16_spans(const void *logits, int64_t rows, int64_t cols, int64_t row_stride,
-                       int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
-                       uint32_t *out_nonfinite_mask, int32_t spans, void *stream);
+/* Launch plans (tf_topk_bf16_with_plan).  Every plan gives identical results. */
+#define TF_TOPK_PLAN_AUTO 0      /* what tf_topk_bf16 picks for the shape */
+#define TF_TOPK_PLAN_SINGLE 1    /* control: one CTA streams each whole row (the
+                                    pages' single-group kernel) */
+#define TF_TOPK_PLAN_CLUSTER2 2  /* each row split into 2/4/8/16 column spans, one */
+#define TF_TOPK_PLAN_CLUSTER4 4  /*   CTA each, inside one thread-block cluster; */
+#define TF_TOPK_PLAN_CLUSTER8 8  /*   the span lists are merged through distributed */
+#define TF_TOPK_PLAN_CLUSTER16 16/*   shared memory */
+#define TF_TOPK_PLAN_STREAM 32   /* persistent CTAs stream equal contiguous ranges
+                                    of the matrix through a TMA ring; rows cut by a
+                                    range boundary are merged by the last CTA to
+                                    finish one of their pieces */
 
-/* The span count tf_topk_bf16 picks for this shape on the current device
- * (>= 1), or a negative TF_TOPK_* status if the shape is invalid. */
+/*
+ * The same operation with the launch plan named by the caller (for
+ * cross-path tests and A/B timing).  `plan` is one of TF_TOPK_PLAN_*;
+ * anything else returns TF_TOPK_ERR_PLAN.
+ */
+int tf_topk_bf16_with_plan(const void *logits, int64_t rows, int64_t cols, int64_t row_stride,
+                           int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                           uint32_t *out_nonfinite_mask, int32_t plan, void *stream);
+
+/* The plan tf_topk_bf16 picks for this shape on the current device (a
+ * TF_TOPK_PLAN_* code), or a negative TF_TOPK_* status if the shape is
+ * invalid. */
 int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k);
+
+/*
+ * Device-side fault check.  Every wait inside the kernels is bounded; a wait
+ * that runs out records a nonzero code in a per-device word and the kernel
+ * returns early (its rows' outputs are then not valid).  This call waits for
+ * the current device to finish its work, returns 0 when no kernel recorded a
+ * fault since the last check, else the fault code (1 = a bulk-copy wait ran
+ * out), and clears it.  A negative value is -TF_TOPK_ERR_CUDA.
+ */
+int tf_topk_device_fault(void);
 
 /* Compile-time constants of the kernels, exported so a host-side check can
  * compare them with the header (the pages' constant tie between kernel and

@@ -27,11 +27,11 @@ def to_numpy(res):
             count.cpu().numpy(), mask.cpu().numpy().view(np.uint32))
 
 
-def gpu_topk(x: np.ndarray, cols: int, k: int, spans: int = 0, offset: int = 0):
+def gpu_topk(x: np.ndarray, cols: int, k: int, plan: int = 0, offset: int = 0):
     from wide_bf16_row_gb300 import topk
 
     view, _keep = device_matrix(x, cols, offset)
-    res = topk.topk_bf16(view, k, spans=spans)
+    res = topk.topk_bf16(view, k, plan=plan)
     out = to_numpy(res)
     del _keep
     return out

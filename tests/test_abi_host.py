@@ -56,8 +56,12 @@ def test_constants_match_header(lib):
     assert c["max_spans"] == macros["TF_TOPK_MAX_SPANS"]
     assert c["cta_threads"] % 32 == 0
     assert c["chunk_columns"] <= 65536 and c["chunk_columns"] % (8 * c["cta_threads"]) == 0
+    for name, val in (("TF_TOPK_PLAN_AUTO", 0), ("TF_TOPK_PLAN_SINGLE", 1), ("TF_TOPK_PLAN_CLUSTER2", 2),
+                      ("TF_TOPK_PLAN_CLUSTER4", 4), ("TF_TOPK_PLAN_CLUSTER8", 8),
+                      ("TF_TOPK_PLAN_CLUSTER16", 16), ("TF_TOPK_PLAN_STREAM", 32)):
+        assert macros[name] == val and val in topk.PLANS
     for i, name in enumerate(["TF_TOPK_OK", "TF_TOPK_ERR_NULL", "TF_TOPK_ERR_SHAPE", "TF_TOPK_ERR_K",
-                              "TF_TOPK_ERR_ALIGN", "TF_TOPK_ERR_SPANS", "TF_TOPK_ERR_DEVICE",
+                              "TF_TOPK_ERR_ALIGN", "TF_TOPK_ERR_PLAN", "TF_TOPK_ERR_DEVICE",
                               "TF_TOPK_ERR_CUDA"]):
         assert macros[name] == i
         assert getattr(topk, name.replace("TF_TOPK_", "")) == i
@@ -67,10 +71,10 @@ FAKE = 0x10000  # a non-NULL, aligned address; guards reject before it is touche
 
 
 def call(lib, logits=FAKE, rows=4, cols=100, stride=100, k=8, idx=FAKE, val=FAKE, count=FAKE,
-         mask=FAKE, spans=None):
-    if spans is None:
+         mask=FAKE, plan=None):
+    if plan is None:
         return lib.tf_topk_bf16(logits, rows, cols, stride, k, idx, val, count, mask, None)
-    return lib.tf_topk_bf16_spans(logits, rows, cols, stride, k, idx, val, count, mask, spans, None)
+    return lib.tf_topk_bf16_with_plan(logits, rows, cols, stride, k, idx, val, count, mask, plan, None)
 
 
 @pytest.mark.parametrize("kwargs,status", [
@@ -81,7 +85,7 @@ def call(lib, logits=FAKE, rows=4, cols=100, stride=100, k=8, idx=FAKE, val=FAKE
     (dict(mask=None), 1),
     (dict(logits=FAKE + 1), 4), (dict(idx=FAKE + 2), 4), (dict(val=FAKE + 1), 4),
     (dict(count=FAKE + 2), 4), (dict(mask=FAKE + 1), 4),
-    (dict(spans=3), 5), (dict(spans=32), 5), (dict(spans=-1), 5),
+    (dict(plan=3), 5), (dict(plan=64), 5), (dict(plan=-1), 5), (dict(plan=17), 5),
 ])
 def test_guards_reject_before_launch(lib, kwargs, status):
     assert call(lib, **kwargs) == status
@@ -89,7 +93,8 @@ def test_guards_reject_before_launch(lib, kwargs, status):
 
 def test_zero_rows_is_a_no_op(lib):
     assert call(lib, rows=0, logits=None, idx=None, val=None, count=None, mask=None) == 0
-    assert call(lib, rows=0, spans=16) == 0
+    assert call(lib, rows=0, plan=16) == 0
+    assert call(lib, rows=0, plan=32) == 0
 
 
 def test_strerror_covers_every_status(lib):

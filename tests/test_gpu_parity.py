@@ -16,7 +16,8 @@ from wide_bf16_row_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-ALL_SPANS = (1, 2, 4, 8, 16)
+# every launch plan: single-CTA control, 2/4/8/16-span clusters, persistent stream
+ALL_PLANS = (1, 2, 4, 8, 16, 32)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -33,11 +34,11 @@ def test_named_workload_full_size(name):
 
 
 @pytest.mark.parametrize("name", ["1x4096_k8", "15x98592_k16", "16x248320_k64_specials"])
-@pytest.mark.parametrize("spans", ALL_SPANS)
-def test_named_workload_every_plan(name, spans):
+@pytest.mark.parametrize("plan", ALL_PLANS)
+def test_named_workload_every_plan(name, plan):
     w = synth.NAMED[name]()
     exp = oracle.topk(w.logits, w.cols, w.k)
-    assert_same(gpu_topk(w.logits, w.cols, w.k, spans=spans), exp, f"{name} spans={spans}")
+    assert_same(gpu_topk(w.logits, w.cols, w.k, plan=plan), exp, f"{name} plan={plan}")
 
 
 @pytest.mark.parametrize("width", synth.SWEEP_WIDTHS)
@@ -62,9 +63,9 @@ def test_edge_grid(cols):
                              special_frac=0.01, dup_frac=0.02)
         for k in (1, 2, 63, 64):
             exp = oracle.topk(x, cols, k)
-            for spans in (0, 1, 16):
-                got = gpu_topk(x, cols, k, spans=spans, offset=offset)
-                assert_same(got, exp, f"cols={cols} stride={stride} off={offset} k={k} spans={spans}")
+            for plan in (0, 1, 16, 32):
+                got = gpu_topk(x, cols, k, plan=plan, offset=offset)
+                assert_same(got, exp, f"cols={cols} stride={stride} off={offset} k={k} plan={plan}")
 
 
 def _tie_rows(cols: int, seed: int) -> np.ndarray:
@@ -92,17 +93,17 @@ def _tie_rows(cols: int, seed: int) -> np.ndarray:
 def test_heavy_ties_and_nan(cols, k):
     x = _tie_rows(cols, seed=cols + k)
     exp = oracle.topk(x, cols, k)
-    for spans in ALL_SPANS:
-        assert_same(gpu_topk(x, cols, k, spans=spans), exp, f"ties cols={cols} k={k} spans={spans}")
+    for plan in ALL_PLANS:
+        assert_same(gpu_topk(x, cols, k, plan=plan), exp, f"ties cols={cols} k={k} plan={plan}")
 
 
 def test_every_plan_agrees_on_random_rows():
     x = synth.mixed_rows(40, 70000, seed=99, row_stride=70003, special_frac=0.002, dup_frac=0.01)
     exp = oracle.topk(x, 70000, 37)
-    for spans in (0,) + ALL_SPANS:
+    for plan in (0,) + ALL_PLANS:
         for offset in (0, 5):
-            assert_same(gpu_topk(x, 70000, 37, spans=spans, offset=offset), exp,
-                        f"spans={spans} off={offset}")
+            assert_same(gpu_topk(x, 70000, 37, plan=plan, offset=offset), exp,
+                        f"plan={plan} off={offset}")
 
 
 def test_repeated_calls_and_streams_are_deterministic():
@@ -152,9 +153,9 @@ def test_gpu_guard_errors_leave_outputs_untouched():
     val = torch.full((4, 8), 77, dtype=torch.int16, device="cuda")
     cnt = torch.full((4,), 5, dtype=torch.int32, device="cuda")
     msk = torch.full((4,), 9, dtype=torch.int32, device="cuda")
-    st = topk.tf_topk_bf16_spans(x.data_ptr(), 4, 100, 100, 8, idx.data_ptr(), val.data_ptr(),
-                                 cnt.data_ptr(), msk.data_ptr(), 3, None)
-    assert st == topk.ERR_SPANS
+    st = topk.tf_topk_bf16_with_plan(x.data_ptr(), 4, 100, 100, 8, idx.data_ptr(), val.data_ptr(),
+                                     cnt.data_ptr(), msk.data_ptr(), 3, None)
+    assert st == topk.ERR_PLAN
     st = topk.tf_topk_bf16(x.data_ptr(), 4, 100, 100, 65, idx.data_ptr(), val.data_ptr(),
                            cnt.data_ptr(), msk.data_ptr(), None)
     assert st == topk.ERR_K
@@ -167,8 +168,6 @@ def test_gpu_guard_errors_leave_outputs_untouched():
 def test_plan_table():
     from wide_bf16_row_gb300 import topk
 
-    assert topk.plan(1, 4095, 8) == 1
-    for rows, cols in ((1, 4096), (15, 98592), (16, 248320), (256, 248320), (1024, 248320)):
-        s = topk.plan(rows, cols, 20)
-        assert s in ALL_SPANS
-        assert (cols + 8) // 8 <= s * 2048 or s == 16
+    for rows, cols in ((1, 100), (1, 4096), (15, 98592), (16, 248320), (256, 248320), (1024, 248320)):
+        assert topk.plan(rows, cols, 20) in ALL_PLANS
+    assert topk.device_fault() == 0

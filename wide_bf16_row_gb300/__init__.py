@@ -8,7 +8,7 @@ of one of its names.
 """
 from __future__ import annotations
 
-__all__ = ["topk_bf16", "tf_topk_bf16", "tf_topk_bf16_spans", "MAX_K", "TopkError"]
+__all__ = ["topk_bf16", "tf_topk_bf16", "tf_topk_bf16_with_plan", "MAX_K", "TopkError", "PLANS"]
 
 
 def __getattr__(name):

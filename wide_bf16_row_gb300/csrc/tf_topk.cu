@@ -9,39 +9,54 @@
 // strides).  The conventions the pages leave open are stated in
 // include/tf_topk.h.
 //
-// Design (one kernel template, one launch per call):
-//   * A CTA owns one column span of one row.  It streams the span through
-//     registers a chunk at a time (kThreads x kVecPerThread 16-byte vectors,
-//     coalesced, read once from HBM).
-//   * Each bf16 becomes an order-preserving 16-bit key in place (two keys per
-//     32-bit register): positive bits b -> b | 0x8000, negative bits b -> ~b.
-//     -0 and +0 land on the neighbouring keys 0x7FFF / 0x8000 and are treated
-//     as one score wherever a threshold or a comparison is taken.
+// Common machinery (both kernels):
+//   * A CTA processes a row a chunk at a time: kThreads x kVecPerThread
+//     16-byte vectors (16384 columns), held in registers as order-preserving
+//     16-bit keys, two per register: positive bits b -> b | 0x8000, negative
+//     bits b -> ~b.  -0 and +0 land on the neighbouring keys 0x7FFF / 0x8000 and
+//     are treated as one score wherever a threshold or a comparison is taken.
 //   * Prefilter: every thread keeps the max key of its elements; each warp finds
 //     the j-th largest of its 32 thread maxima (j = ceil(k / warps)); the
-//     minimum T over warps is a value that at least k elements reach, so the
-//     chunk's top-k lies in {key >= T}.  Only those candidates (typically a few
-//     times k out of 16384) touch shared memory.
-//   * The candidates are ranked exactly with a 32-bit composite
-//     (key << 16 | ~local column), which is unique, so every rank is distinct.
-//     Rows with heavy ties (e.g. all zeros) overflow the candidate buffer and
-//     take an exact radix path instead: a binary search for the k-th key, then
-//     the lowest columns among the threshold ties, found by a block scan in
-//     column order.
-//   * A CTA's running list (<= k entries, 64-bit composites holding key,
-//     column and the original bits) is merged chunk by chunk.
-//   * spans > 1: the CTAs of one row form a thread-block cluster; each pushes
-//     its sorted list into the leader CTA's shared memory (distributed shared
-//     memory) and the leader merges the lists pairwise (a tournament tree) and
-//     writes the row.  spans == 1 is the single-CTA control path.
-// There is no global scratch, no atomic on global memory and no spin-wait: the
-// only cross-CTA synchronisation is the hardware cluster barrier.
+//     minimum T over warps is reached by at least k elements, so the chunk's
+//     top-k lies in {key >= T}.  Only those candidates (typically a few times k
+//     out of 16384) touch shared memory.
+//   * Candidates are ranked exactly with a unique 32-bit composite
+//     (key << 16 | ~chunk-local column).  Chunks with heavy ties (e.g. an
+//     all-zero row) overflow the candidate buffer and take an exact path: a
+//     binary search for the k-th key, then the lowest columns among the ties at
+//     that key, ranked by a block scan in column order.
+//   * A running list (<= k entries, 64-bit: key | ~column | original bits)
+//     absorbs the chunks of a row piece; pieces are merged pairwise (the
+//     pages' tournament) in the same order.
+//
+// Kernel 1, topk_stream_kernel (the default plan): a persistent grid of two
+// CTAs per SM.  The rows x vectors space is cut into equal contiguous ranges,
+// one per CTA, so every SM gets the same number of bytes whatever the shape.
+// Each CTA streams its range through a 3-stage shared-memory ring filled by
+// TMA bulk copies (cp.async.bulk + mbarrier): two chunks are in flight while
+// one is selected.  A row cut by a range boundary leaves one partial list per
+// piece in a small scratch area; the last CTA to finish a piece of that row
+// (an atomic ticket) merges them and writes the row.  With one range per row
+// the same kernel is the single-CTA control path.
+//
+// Kernel 2, topk_cluster_kernel<S>: S CTAs of a thread-block cluster split one
+// row into S spans, load with 16-byte register loads, and merge through
+// distributed shared memory in the leader CTA.  Kept as a measured
+// alternative plan.
+//
+// No wait is unbounded: mbarrier waits give up after kWaitLimit polls, record
+// a fault code in a device word, drain their own copies (again bounded) and
+// return.  Nothing waits on another CTA: cross-CTA hand-off is the hardware
+// cluster barrier or the last-arriver ticket.
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <map>
 #include <mutex>
+#include <thread>
+#include <utility>
 
 #include "tf_topk.h"
 
@@ -56,7 +71,12 @@ constexpr int kChunkVecs = kThreads * kVecPerThread; // 2048 vectors
 constexpr int kChunkCols = kChunkVecs * 8;           // 16384 columns
 constexpr int kMaxK = TF_TOPK_MAX_K;
 constexpr int kMaxSpans = TF_TOPK_MAX_SPANS;
-constexpr int kCandCap = 256; // candidates ranked directly (one per thread)
+constexpr int kCandCap = 256;        // candidates ranked directly (one per thread)
+constexpr int kStages = 3;           // TMA ring depth of the stream kernel
+constexpr int kStreamCtasPerSm = 2;  // resident stream CTAs per SM
+constexpr int kMinVecsPerCta = 1024; // smallest range a stream CTA is given
+constexpr int kMaxPieces = kMaxSpans;// most pieces a stream row is cut into
+constexpr uint32_t kWaitLimit = 1u << 22;
 
 // The constant ties the pages ask for: a change to one of these fails the build.
 static_assert(kThreads % 32 == 0 && kThreads >= 64, "whole warps");
@@ -64,8 +84,9 @@ static_assert(kChunkCols <= 65536, "chunk-local column must fit the 16-bit compo
 static_assert(kCandCap <= kThreads, "rank pass gives each candidate its own thread");
 static_assert(kMaxK <= kCandCap, "exact path writes k candidates");
 static_assert((kMaxK + kWarps - 1) / kWarps <= 32, "per-warp order statistic needs j <= 32");
-static_assert(kMaxSpans == 16 && (kMaxSpans & (kMaxSpans - 1)) == 0, "merge tree over 2^n spans");
+static_assert(kMaxSpans == 16 && (kMaxSpans & (kMaxSpans - 1)) == 0, "merge tree over 2^n lists");
 static_assert(kMaxK == 64, "header and kernels agree on max_k");
+static_assert(kStages >= 2, "a ring needs two stages");
 
 constexpr uint32_t kEmptyVal = 0x7FC0;
 constexpr uint32_t kKeyPosInf = 0xFF80;
@@ -73,23 +94,31 @@ constexpr uint32_t kKeyNegInf = 0x007F;
 constexpr uint32_t kKeyNegZero = 0x7FFF;
 constexpr uint32_t kKeyPosZero = 0x8000;
 
-struct __align__(16) Smem {
-    uint32_t cand[kCandCap + 4];      // chunk candidates, 32-bit composites (+ zero pad)
-    uint16_t cand_raw[kCandCap];      // their original bf16 bits
-    uint64_t list[3][kMaxK];          // running list, chunk list, merge output
-    uint64_t gather[kMaxSpans][kMaxK];     // leader: the spans' lists
-    uint64_t gather2[kMaxSpans / 2][kMaxK];// leader: merge-tree ping-pong
-    int32_t glen[kMaxSpans];
-    int32_t glen2[kMaxSpans / 2];
-    uint32_t gflags[kMaxSpans];
+// Device fault word: 0, or the first fault code a kernel recorded.
+constexpr uint32_t kFaultWaitTimeout = 1;
+__device__ uint32_t g_fault;
+
+struct __align__(16) SmemCore {
+    uint32_t cand[kCandCap + 4];            // chunk candidates, 32-bit composites (+ zero pad)
+    uint16_t cand_raw[kCandCap];            // their original bf16 bits
+    uint64_t list[3][kMaxK];                // running list, chunk list, merge output
     uint32_t warp_t[kWarps];
     uint32_t red[2][kWarps];
     uint32_t scan[kWarps][4];
-    uint32_t keys[kChunkCols / 2];    // exact path: the chunk's keys, two per word, column order
+    uint64_t mbar[kStages];
     uint32_t n_cand;
     uint32_t flags;
     uint32_t kmax;
-    int32_t run_len;
+    uint32_t ticket;
+};
+
+// The cluster leader's gather area: every span CTA pushes its list here.
+struct __align__(16) SmemGather {
+    uint64_t gather[kMaxSpans][kMaxK];      // lists being merged
+    uint64_t gather2[kMaxSpans / 2][kMaxK]; // merge-tree ping-pong
+    int32_t glen[kMaxSpans];
+    int32_t glen2[kMaxSpans / 2];
+    uint32_t gflags[kMaxSpans];
 };
 
 // ---------------------------------------------------------------- bit helpers
@@ -116,11 +145,6 @@ __device__ __forceinline__ uint32_t keys_from_raw2(uint32_t x)
     uint32_t s;
     asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(s) : "r"(x));
     return x ^ (s | 0x80008000u);
-}
-
-__device__ __forceinline__ uint32_t key_from_raw(uint32_t b)
-{
-    return b ^ ((b & 0x8000u) ? 0xFFFFu : 0x8000u);
 }
 
 __device__ __forceinline__ uint32_t raw_from_key(uint32_t key)
@@ -197,7 +221,7 @@ __device__ __forceinline__ void merge_lists(const uint64_t *a, int la, const uin
     }
 }
 
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, Smem &sm, int parity)
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, SmemCore &sm, int parity)
 {
     v = __reduce_add_sync(0xFFFFFFFFu, v);
     if ((threadIdx.x & 31) == 0) sm.red[parity][threadIdx.x >> 5] = v;
@@ -208,7 +232,7 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, Smem &sm, int parity)
     return s;
 }
 
-__device__ __forceinline__ void push_candidate(Smem &sm, uint32_t key, int local)
+__device__ __forceinline__ void push_candidate(SmemCore &sm, uint32_t key, int local)
 {
     const uint32_t slot = atomicAdd(&sm.n_cand, 1u);
     if (slot < (uint32_t)kCandCap) {
@@ -217,13 +241,14 @@ __device__ __forceinline__ void push_candidate(Smem &sm, uint32_t key, int local
     }
 }
 
-// Keys of sm.keys whose score is >= the score of key t (t >= 1), this thread's share.
-__device__ __forceinline__ uint32_t count_at_least(const Smem &sm, uint32_t t)
+// Keys of the staged chunk whose score is >= the score of key t (t >= 1), this
+// thread's share.
+__device__ __forceinline__ uint32_t count_at_least(const uint32_t *keys, uint32_t t)
 {
     const uint32_t f = key_floor(t);
     uint32_t c = 0;
     for (int w = threadIdx.x; w < kChunkCols / 2; w += kThreads) {
-        const uint32_t k2 = sm.keys[w];
+        const uint32_t k2 = keys[w];
         c += (k2 & 0xFFFFu) >= f;
         c += (k2 >> 16) >= f;
     }
@@ -232,16 +257,16 @@ __device__ __forceinline__ uint32_t count_at_least(const Smem &sm, uint32_t t)
 
 // Exact selection for a chunk whose candidate set {key >= t_floor} is larger
 // than the candidate buffer (heavy ties, e.g. an all-zero row).  The chunk's
-// keys have been staged in sm.keys in column order (0 = not a candidate).
+// keys have been staged in `keys` in column order (0 = not a candidate).
 // Writes exactly k candidates -- the chunk's top-k within that set -- into
 // sm.cand.  Block-uniform; every thread calls it.
-__device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
+__device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor, int k, SmemCore &sm)
 {
     const int tid = threadIdx.x;
     // 1. K* = the largest canonical key that at least k elements reach.
     uint32_t my_max = 0;
     for (int w = tid; w < kChunkCols / 2; w += kThreads)
-        my_max = max(my_max, max(sm.keys[w] & 0xFFFFu, sm.keys[w] >> 16));
+        my_max = max(my_max, max(keys[w] & 0xFFFFu, keys[w] >> 16));
     if (tid == 0) sm.kmax = 0;
     __syncthreads();
     atomicMax(&sm.kmax, canon(my_max));
@@ -251,7 +276,7 @@ __device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
     int parity = 0;
     while (hi - lo > 1) {
         const uint32_t mid = (lo + hi) >> 1;
-        const uint32_t c = block_sum(count_at_least(sm, mid), sm, parity);
+        const uint32_t c = block_sum(count_at_least(keys, mid), sm, parity);
         parity ^= 1;
         if (c >= (uint32_t)k)
             lo = mid;
@@ -260,7 +285,7 @@ __device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
     }
     const uint32_t kstar = lo;
     const uint32_t above =
-        (kstar >= kKeyPosInf) ? 0u : block_sum(count_at_least(sm, kstar + 1), sm, parity);
+        (kstar >= kKeyPosInf) ? 0u : block_sum(count_at_least(keys, kstar + 1), sm, parity);
     const uint32_t need = (uint32_t)k - above; // ties at K* to take, lowest columns first
 
     // 2. Each thread owns a contiguous run of columns; an exclusive scan of the
@@ -269,8 +294,8 @@ __device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
     const int w0 = tid * kWordsPerThread;
     uint32_t ties = 0;
     for (int w = w0; w < w0 + kWordsPerThread; ++w) {
-        ties += canon(sm.keys[w] & 0xFFFFu) == kstar;
-        ties += canon(sm.keys[w] >> 16) == kstar;
+        ties += canon(keys[w] & 0xFFFFu) == kstar;
+        ties += canon(keys[w] >> 16) == kstar;
     }
     const int lane = tid & 31, warp = tid >> 5;
     uint32_t incl = ties;
@@ -289,7 +314,7 @@ __device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
     for (int w = w0; w < w0 + kWordsPerThread; ++w) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t key = h ? (sm.keys[w] >> 16) : (sm.keys[w] & 0xFFFFu);
+            const uint32_t key = h ? (keys[w] >> 16) : (keys[w] & 0xFFFFu);
             if (key == 0) continue;
             const uint32_t c = canon(key);
             if (c > kstar) {
@@ -303,7 +328,534 @@ __device__ __noinline__ void exact_select(uint32_t t_floor, int k, Smem &sm)
     __syncthreads();
 }
 
-// ---------------------------------------------------------------- cluster barrier
+// Where a chunk sits in its row.  Vector v covers row columns [8v - m, 8v - m + 8);
+// vectors [vfull0, vfull1) lie wholly inside [0, cols).
+struct ChunkGeom {
+    const uint16_t *rowp;
+    int32_t cols, m, vfull0, vfull1;
+    int32_t cbeg, cend; // chunk vectors
+};
+
+__device__ __forceinline__ ChunkGeom row_geometry(const uint16_t *rowp, int32_t cols)
+{
+    ChunkGeom g;
+    g.rowp = rowp;
+    g.cols = cols;
+    g.m = (int32_t)((reinterpret_cast<uintptr_t>(rowp) >> 1) & 7);
+    g.vfull0 = g.m ? 1 : 0;
+    g.vfull1 = (cols + g.m) >> 3;
+    g.cbeg = g.cend = 0;
+    return g;
+}
+
+
+// Element-wise load of an edge vector (a vector that straddles a row end):
+// columns outside [0, cols) read as 0xFFFF, whose key is 0 (never selected).
+__device__ __noinline__ uint4 load_edge_vector(const uint16_t *rowp, int32_t cols, int32_t m, int32_t v)
+{
+    uint32_t w4[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int32_t c0 = v * 8 + 2 * w - m;
+        const uint32_t lo = (c0 >= 0 && c0 < cols) ? rowp[c0] : 0xFFFFu;
+        const uint32_t hi = (c0 + 1 >= 0 && c0 + 1 < cols) ? rowp[c0 + 1] : 0xFFFFu;
+        w4[w] = lo | (hi << 16);
+    }
+    return make_uint4(w4[0], w4[1], w4[2], w4[3]);
+}
+
+// The exact key pass for one thread whose chunk slice holds a column outside
+// the row or a non-finite value.  Its keys sit in its own stage slots
+// (vector i at stage[i * kThreads + tid]); columns outside the row and NaNs
+// become key 0 and the row's non-finite flags are recorded.  Returns the
+// thread's max key over what remains.
+__device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_t cols, int nvalid,
+                                          SmemCore &sm)
+{
+    const int tid = threadIdx.x;
+    uint32_t tmax = 0, flags = 0;
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int lv = i * kThreads + tid;
+        if (lv >= nvalid) continue;
+        uint4 q = stage[lv];
+        uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        for (int w = 0; w < 4; ++w) {
+            uint32_t out = 0;
+            for (int h = 0; h < 2; ++h) {
+                const int32_t c = col_base + lv * 8 + 2 * w + h;
+                uint32_t key = (qw[w] >> (16 * h)) & 0xFFFFu;
+                if (c < 0 || c >= cols) {
+                    key = 0;
+                } else if (key > kKeyPosInf || key < kKeyNegInf) {
+                    flags |= 1u; // NaN
+                    key = 0;
+                } else if (key == kKeyPosInf) {
+                    flags |= 2u;
+                } else if (key == kKeyNegInf) {
+                    flags |= 4u;
+                }
+                tmax = max(tmax, key);
+                out |= key << (16 * h);
+            }
+            qw[w] = out;
+        }
+        stage[lv] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    }
+    if (flags) atomicOr(&sm.flags, flags);
+    return tmax;
+}
+
+// Keys of one chunk.  kv holds the raw words of this thread's vectors (vector
+// i is chunk vector i * kThreads + tid; vectors past the chunk end are 0); on
+// return it holds their keys (0 where no score may be selected), and the
+// thread's max key is returned.  kFull: every vector of the chunk lies wholly
+// inside the row (no predicates).  `stage` is the chunk's 32 KB of shared
+// memory, this thread's slots of which the rare exact pass may use.
+template <bool kFull>
+__device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4], int nvalid,
+                                               int32_t col_base, int32_t cols, uint4 *stage, SmemCore &sm)
+{
+    const int tid = threadIdx.x;
+    uint32_t mx = 0, mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+        if (kFull || i * kThreads + tid < nvalid) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t key = keys_from_raw2(kv[i][w]);
+                kv[i][w] = key;
+                mx = max_u16x2(mx, key);
+                mn = min_u16x2(mn, key);
+            }
+        }
+    }
+    uint32_t tmax = max(mx & 0xFFFFu, mx >> 16);
+    const uint32_t tmin = min(mn & 0xFFFFu, mn >> 16);
+
+    // ---- exact key pass (columns outside the row, NaN, +-inf), through shared memory
+    if (tmax >= kKeyPosInf || tmin <= kKeyNegInf) {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i)
+            stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+        tmax = fix_keys(stage, col_base, cols, nvalid, sm);
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const uint4 q = stage[i * kThreads + tid];
+            kv[i][0] = q.x;
+            kv[i][1] = q.y;
+            kv[i][2] = q.z;
+            kv[i][3] = q.w;
+        }
+    }
+    return tmax;
+}
+
+// Selection for one chunk whose keys are in kv (see chunk_keys) with this
+// thread's max key tmax: the row piece's running list (run_i, run_len)
+// absorbs the chunk's top-k.  Block-uniform: every thread calls it.
+__device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, int nvalid,
+                                             int32_t col_base, int k, SmemCore &sm, uint4 *stage,
+                                             int &run_i, int &chunk_i, int &free_i, int &run_len)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // ---- prefilter threshold.  The fw warps whose 32 lanes all hold data each
+    //      find the j-th largest of their lanes' maxima, j = ceil(k / fw); the
+    //      minimum t0 over them is reached by at least fw * j >= k elements.
+    //      With no such bound (a tiny chunk, or a warp without j positive
+    //      maxima) t0 = 0 and every element is a candidate.
+    const int fw = min(nvalid, kThreads) / 32;
+    const int j = fw ? (k + fw - 1) / fw : 33;
+    {
+        uint32_t tw = 0xFFFFu; // warps without a full set of lanes do not bound
+        if (warp < fw) {
+            tw = 0;
+            if (j <= 32) {
+                uint32_t v = tmax, cnt = 0;
+                for (int it = 0; it < j; ++it) {
+                    const uint32_t mval = __reduce_max_sync(0xFFFFFFFFu, v);
+                    if (mval == 0) break;
+                    cnt += __popc(__ballot_sync(0xFFFFFFFFu, v == mval));
+                    if (cnt >= (uint32_t)j) {
+                        tw = mval;
+                        break;
+                    }
+                    if (v == mval) v = 0;
+                }
+            }
+        }
+        if (lane == 0) sm.warp_t[warp] = tw;
+    }
+    if (tid == 0) sm.n_cand = 0;
+    __syncthreads();
+    uint32_t t0 = (fw == 0 || j > 32) ? 0u : 0xFFFFu;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
+    uint32_t t_floor = max(key_floor(t0), 1u);
+    if (run_len == k) {
+        // a new entry must beat the running k-th strictly (it has a higher column)
+        const uint32_t kth = (uint32_t)(sm.list[run_i][k - 1] >> 48);
+        t_floor = max(t_floor, kth + 1);
+    }
+
+    // ---- candidates: only threads whose max reaches t_floor hold any; each
+    //      such thread spills its keys, and its warp scans them one word per lane
+    const bool hit = tmax >= t_floor;
+    if (hit) {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i)
+            stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+    }
+    __syncwarp();
+    for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits; hits &= hits - 1) {
+        const int src = warp * 32 + __ffs(hits) - 1;
+        const int lv = (lane >> 2) * kThreads + src;
+        const uint32_t key2 = reinterpret_cast<const uint32_t *>(stage)[lv * 4 + (lane & 3)];
+        const int local = lv * 8 + 2 * (lane & 3);
+        if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local);
+        if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1);
+    }
+    __syncthreads();
+    uint32_t n = sm.n_cand;
+    if (n > (uint32_t)kCandCap) {
+        // heavy ties: stage every key in column order (below t_floor -> 0) and
+        // select exactly
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            uint32_t q[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t lo = kv[i][w] & 0xFFFFu, hi = kv[i][w] >> 16;
+                q[w] = (lo >= t_floor ? lo : 0u) | ((hi >= t_floor ? hi : 0u) << 16);
+            }
+            stage[i * kThreads + tid] = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+        __syncthreads();
+        exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
+        n = sm.n_cand; // == k
+    }
+    // the stage may next be written by a bulk copy (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    // ---- rank the candidates: rank = number of larger composites
+    if (tid < (int)n) {
+        const uint32_t e = sm.cand[tid];
+        uint32_t rank = 0;
+        const uint4 *c4 = reinterpret_cast<const uint4 *>(sm.cand);
+        const uint32_t nq = n >> 2;
+        for (uint32_t u = 0; u < nq; ++u) {
+            const uint4 q = c4[u];
+            rank += (q.x > e) + (q.y > e) + (q.z > e) + (q.w > e);
+        }
+        for (uint32_t u = nq * 4; u < n; ++u) rank += sm.cand[u] > e;
+        if (rank < (uint32_t)k) sm.list[chunk_i][rank] = entry_from_cand(e, sm.cand_raw[tid], col_base);
+    }
+    __syncthreads();
+    const int chunk_len = min((int)n, k);
+    if (run_len == 0) {
+        const int t = run_i;
+        run_i = chunk_i;
+        chunk_i = t;
+    } else if (chunk_len > 0) {
+        merge_lists(sm.list[run_i], run_len, sm.list[chunk_i], chunk_len, sm.list[free_i], k);
+        const int t = run_i;
+        run_i = free_i;
+        free_i = t;
+    }
+    run_len = min(k, run_len + chunk_len);
+    // the next reader of the running list is behind a barrier of the caller
+}
+
+// Merge sm.gather[0..nl) (nl a power of two, lengths in sm.glen) pairwise into
+// one list; returns it (in sm.gather or sm.gather2) and its length.
+__device__ __forceinline__ const uint64_t *merge_tree(SmemGather &sm, int nl, int k, int &out_len)
+{
+    const int tid = threadIdx.x;
+    uint64_t(*src)[kMaxK] = sm.gather;
+    uint64_t(*dst)[kMaxK] = sm.gather2;
+    int32_t *src_len = sm.glen;
+    int32_t *dst_len = sm.glen2;
+    for (; nl > 1; nl >>= 1) {
+        for (int t = tid; t < nl * kMaxK; t += kThreads) {
+            const int l = t / kMaxK, pos = t % kMaxK;
+            if (pos >= src_len[l]) continue;
+            const uint64_t x = src[l][pos];
+            const int p = l ^ 1;
+            const int out = pos + count_greater(src[p], src_len[p], x);
+            if (out < k) dst[l >> 1][out] = x;
+        }
+        if (tid < nl / 2) dst_len[tid] = min(k, src_len[2 * tid] + src_len[2 * tid + 1]);
+        __syncthreads();
+        uint64_t(*tl)[kMaxK] = src;
+        src = dst;
+        dst = tl;
+        int32_t *tlen = src_len;
+        src_len = dst_len;
+        dst_len = tlen;
+    }
+    out_len = src_len[0];
+    return src[0];
+}
+
+__device__ __forceinline__ void write_row(int64_t row, const uint64_t *list, int len, uint32_t flags,
+                                          int k, int32_t *out_idx, uint16_t *out_val,
+                                          int32_t *out_count, uint32_t *out_mask)
+{
+    for (int t = threadIdx.x; t < k; t += kThreads) {
+        const int64_t o = row * k + t;
+        if (t < len) {
+            const uint64_t e = list[t];
+            out_idx[o] = entry_col(e);
+            out_val[o] = (uint16_t)(e & 0xFFFFu);
+        } else {
+            out_idx[o] = -1;
+            out_val[o] = (uint16_t)kEmptyVal;
+        }
+    }
+    if (threadIdx.x == 0) {
+        out_count[row] = len;
+        out_mask[row] = flags;
+    }
+}
+
+// ---------------------------------------------------------------- mbarrier / TMA
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true once the phase with this parity has completed, false
+// after kWaitLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                     "r"(smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- stream kernel
+
+__global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
+topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
+                   int32_t nvr, int64_t total, int64_t per, int32_t *__restrict__ out_idx,
+                   uint16_t *__restrict__ out_val, int32_t *__restrict__ out_count,
+                   uint32_t *__restrict__ out_mask, uint64_t *__restrict__ partials,
+                   uint32_t *__restrict__ tickets)
+{
+    extern __shared__ __align__(128) uint8_t dsmem[];
+    uint4 *stages = reinterpret_cast<uint4 *>(dsmem);
+    SmemCore &sm = *reinterpret_cast<SmemCore *>(dsmem + (size_t)kStages * kChunkVecs * 16);
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const int64_t g0 = b * per;
+    const int64_t g1 = min(total, g0 + per);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&sm.mbar[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // producer (thread 0): the bulk copies of chunk number `issued`, walking the
+    // range [g0, g1) row by row without divisions
+    const int64_t row0 = g0 / nvr;
+    int64_t pg = g0, prow = row0;
+    int32_t pcb = (int32_t)(g0 - row0 * nvr);
+    int issued = 0;
+    auto issue_next = [&]() {
+        if (pg >= g1) return;
+        int32_t pce = pcb + kChunkVecs;
+        if (pce > nvr) pce = nvr;
+        if ((int64_t)(pce - pcb) > g1 - pg) pce = pcb + (int32_t)(g1 - pg);
+        const uint16_t *rowp = logits + prow * row_stride;
+        const int32_t m = (int32_t)((reinterpret_cast<uintptr_t>(rowp) >> 1) & 7);
+        const int32_t f0 = max(pcb, m ? 1 : 0);
+        const int32_t f1 = min(pce, (cols + m) >> 3);
+        const int s = issued % kStages;
+        const uint32_t bytes = f1 > f0 ? (uint32_t)(f1 - f0) * 16u : 0u;
+        mbar_expect_tx(&sm.mbar[s], bytes);
+        if (bytes)
+            bulk_load(stages + (size_t)s * kChunkVecs + (f0 - pcb),
+                      reinterpret_cast<const uint4 *>(rowp - m) + f0, bytes, &sm.mbar[s]);
+        pg += pce - pcb;
+        if (pce == nvr) {
+            ++prow;
+            pcb = 0;
+        } else {
+            pcb = pce;
+        }
+        ++issued;
+    };
+    if (tid == 0)
+        for (int s = 0; s < kStages - 1; ++s) issue_next();
+
+    int c = 0; // chunks consumed
+    bool aborted = false;
+    int64_t g = g0;
+    int64_t row = row0; // the consumer's own cursor (thread 0's producer cursor runs ahead)
+    int32_t vb = (int32_t)(g0 - row0 * nvr);
+    while (g < g1 && !aborted) {
+        const int32_t ve = (int32_t)min((int64_t)nvr, (int64_t)vb + (g1 - g));
+        const ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
+        if (tid == 0) sm.flags = 0;
+        int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
+
+        for (int32_t cb = vb; cb < ve; cb += kChunkVecs) {
+            const int32_t ce = min(ve, cb + kChunkVecs);
+            const int s = c % kStages;
+            // one thread waits for the chunk's bulk copy; the barrier hands it on
+            bool ok = true;
+            if (tid == 0) ok = mbar_wait(&sm.mbar[s], (uint32_t)((c / kStages) & 1));
+            if (__syncthreads_or(!ok)) {
+                aborted = true;
+                break;
+            }
+            if (tid == 0) {
+                // every thread is past the previous chunk: refill its stage
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue_next();
+            }
+            uint4 *st = stages + (size_t)s * kChunkVecs;
+            const int nvalid = ce - cb;
+            const int32_t col_base = cb * 8 - geo.m;
+            uint32_t kv[kVecPerThread][4];
+            uint32_t tmax;
+            if (nvalid == kChunkVecs && cb >= geo.vfull0 && ce <= geo.vfull1) {
+#pragma unroll
+                for (int i = 0; i < kVecPerThread; ++i) {
+                    const uint4 q = st[i * kThreads + tid];
+                    kv[i][0] = q.x;
+                    kv[i][1] = q.y;
+                    kv[i][2] = q.z;
+                    kv[i][3] = q.w;
+                }
+                tmax = chunk_keys<true>(kv, nvalid, col_base, cols, st, sm);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVecPerThread; ++i) {
+                    const int lv = i * kThreads + tid;
+                    uint4 q = make_uint4(0, 0, 0, 0);
+                    if (lv < nvalid) {
+                        const int32_t v = cb + lv;
+                        q = (v >= geo.vfull0 && v < geo.vfull1) ? st[lv]
+                                                               : load_edge_vector(geo.rowp, cols, geo.m, v);
+                    }
+                    kv[i][0] = q.x;
+                    kv[i][1] = q.y;
+                    kv[i][2] = q.z;
+                    kv[i][3] = q.w;
+                }
+                tmax = chunk_keys<false>(kv, nvalid, col_base, cols, st, sm);
+            }
+            select_chunk(kv, tmax, nvalid, col_base, k, sm, st, run_i, chunk_i, free_i, run_len);
+            ++c;
+        }
+        if (aborted) break;
+        __syncthreads(); // the running list is complete
+
+        // ---- end of a row piece
+        const int len = run_len;
+        const uint32_t flags = sm.flags;
+        if (vb == 0 && ve == nvr) {
+            write_row(row, sm.list[run_i], len, flags, k, out_idx, out_val, out_count, out_mask);
+        } else {
+            // publish this piece's list, then take a ticket for the row
+            const int slot = (g0 / nvr == row) ? 0 : 1;
+            uint64_t *mine = partials + (size_t)(b * 2 + slot) * (kMaxK + 1);
+            for (int t = tid; t < len; t += kThreads) mine[1 + t] = sm.list[run_i][t];
+            if (tid == 0) mine[0] = (uint64_t)(uint32_t)len | ((uint64_t)flags << 32);
+            __syncthreads();
+            const int64_t first = (row * nvr) / per;
+            const int64_t last = min((int64_t)gridDim.x - 1, ((row + 1) * nvr - 1) / per);
+            const int np = (int)(last - first + 1);
+            if (tid == 0) {
+                __threadfence();
+                sm.ticket = atomicAdd(&tickets[first], 1u);
+            }
+            __syncthreads();
+            if (sm.ticket == (uint32_t)(np - 1)) {
+                // last piece in: fold every piece of this row into one list
+                __threadfence();
+                int rl = 0, ri = 0, ci = 1, fi = 2;
+                uint32_t fl = 0;
+                for (int j = 0; j < np; ++j) {
+                    const int64_t cta = first + j;
+                    const int sl = ((cta * per) / nvr == row) ? 0 : 1;
+                    const uint64_t *p = partials + (size_t)(cta * 2 + sl) * (kMaxK + 1);
+                    const uint64_t hdr = __ldcg(p);
+                    const int lj = (int)(uint32_t)hdr;
+                    fl |= (uint32_t)(hdr >> 32);
+                    uint64_t *dst = sm.list[rl == 0 ? ri : ci];
+                    for (int t = tid; t < lj; t += kThreads) dst[t] = __ldcg(p + 1 + t);
+                    __syncthreads();
+                    if (rl == 0) {
+                        rl = lj;
+                    } else if (lj > 0) {
+                        merge_lists(sm.list[ri], rl, sm.list[ci], lj, sm.list[fi], k);
+                        const int t = ri;
+                        ri = fi;
+                        fi = t;
+                        rl = min(k, rl + lj);
+                    }
+                    __syncthreads();
+                }
+                write_row(row, sm.list[ri], rl, fl, k, out_idx, out_val, out_count, out_mask);
+                if (tid == 0) tickets[first] = 0; // ready for the next call
+            }
+            __syncthreads();
+        }
+        g += ve - vb;
+        if (ve == nvr) {
+            ++row;
+            vb = 0;
+        } else {
+            vb = ve;
+        }
+    }
+
+    if (aborted) {
+        if (tid == 0) {
+            atomicCAS(&g_fault, 0u, kFaultWaitTimeout);
+            // drain this CTA's copies still in flight, each with a bounded wait
+            for (int q = c; q < issued; ++q) mbar_wait(&sm.mbar[q % kStages], (uint32_t)((q / kStages) & 1));
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- cluster kernel
 
 __device__ __forceinline__ void cluster_arrive_relaxed()
 {
@@ -320,298 +872,85 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- the kernel
-
-// grid.x = rows * S; with S > 1 the launch groups each row's S CTAs into one
-// cluster (cluster rank == span).
+// grid.x = rows * S; the launch groups each row's S CTAs into one cluster
+// (cluster rank == span).
 template <int S>
 __global__ void __launch_bounds__(kThreads, 4)
-topk_rows_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
-                 int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
-                 int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
+topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
+                    int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
+                    int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
 {
-    __shared__ Smem sm;
+    __shared__ SmemCore sm;
+    __shared__ SmemGather sg;
+    __shared__ uint4 keys[kChunkVecs];
     const int tid = threadIdx.x;
-    const int span = (S > 1) ? (int)(blockIdx.x % S) : 0;
+    const int span = (int)(blockIdx.x % S);
     const int64_t row = (int64_t)(blockIdx.x / S);
 
-    if constexpr (S > 1) cluster_arrive_relaxed(); // paired with the wait before DSMEM use
+    cluster_arrive_relaxed(); // paired with the wait before DSMEM use
 
-    const uint16_t *rowp = logits + row * row_stride;
-    const int32_t m = (int32_t)((reinterpret_cast<uintptr_t>(rowp) >> 1) & 7); // elements before the 16-B boundary
-    const uint4 *vbase = reinterpret_cast<const uint4 *>(rowp - m);
-    const int32_t nvec = (cols + m + 7) >> 3;   // vectors touching [0, cols)
-    const int32_t vfull0 = m ? 1 : 0;           // vectors wholly inside [0, cols)
-    const int32_t vfull1 = (cols + m) >> 3;     //   are [vfull0, vfull1)
+    ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
+    const uint4 *vbase = reinterpret_cast<const uint4 *>(geo.rowp - geo.m);
+    const int32_t nvec = (cols + geo.m + 7) >> 3;
     const int32_t per_span = (nvec + S - 1) / S;
     const int32_t v_begin = min(nvec, span * per_span);
     const int32_t v_end = min(nvec, v_begin + per_span);
 
-    if (tid == 0) {
-        sm.flags = 0;
-        sm.run_len = 0;
-    }
+    if (tid == 0) sm.flags = 0;
     __syncthreads();
-    int run_i = 0, chunk_i = 1, free_i = 2;
-    const int j = (k + kWarps - 1) / kWarps;
+    int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
 
     for (int32_t cbeg = v_begin; cbeg < v_end; cbeg += kChunkVecs) {
-        const int32_t cend = min(v_end, cbeg + kChunkVecs);
-        const int32_t col_base = cbeg * 8 - m;
-
-        // ---- load: full vectors by 16-byte loads, edge vectors element-wise
+        geo.cbeg = cbeg;
+        geo.cend = min(v_end, cbeg + kChunkVecs);
+        const int nvalid = geo.cend - cbeg;
+        const int32_t col_base = cbeg * 8 - geo.m;
         uint32_t kv[kVecPerThread][4];
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i) {
-            const int32_t v = cbeg + i * kThreads + tid;
-            if (v < cend && v >= vfull0 && v < vfull1) {
-                const uint4 q = ld_stream(vbase + v);
-                kv[i][0] = q.x;
-                kv[i][1] = q.y;
-                kv[i][2] = q.z;
-                kv[i][3] = q.w;
-            } else if (v < cend) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const int32_t c0 = v * 8 + 2 * w - m;
-                    const uint32_t lo = (c0 >= 0 && c0 < cols) ? rowp[c0] : 0xFFFFu;
-                    const uint32_t hi = (c0 + 1 >= 0 && c0 + 1 < cols) ? rowp[c0 + 1] : 0xFFFFu;
-                    kv[i][w] = lo | (hi << 16);
-                }
-            } else {
-#pragma unroll
-                for (int w = 0; w < 4; ++w) kv[i][w] = 0;
+            const int lv = i * kThreads + tid;
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (lv < nvalid) {
+                const int32_t v = cbeg + lv;
+                q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
+                                                       : load_edge_vector(geo.rowp, cols, geo.m, v);
             }
+            kv[i][0] = q.x;
+            kv[i][1] = q.y;
+            kv[i][2] = q.z;
+            kv[i][3] = q.w;
         }
-
-        // ---- keys, thread max/min over the full vectors
-        uint32_t mx = 0, mn = 0xFFFFFFFFu;
-        bool edge = false;
-#pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            const int32_t v = cbeg + i * kThreads + tid;
-            if (v < cend && v >= vfull0 && v < vfull1) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t key = keys_from_raw2(kv[i][w]);
-                    kv[i][w] = key;
-                    mx = max_u16x2(mx, key);
-                    mn = min_u16x2(mn, key);
-                }
-            } else if (v < cend) {
-                edge = true;
-            }
-        }
-        uint32_t tmax = max(mx & 0xFFFFu, mx >> 16);
-        const uint32_t tmin = min(mn & 0xFFFFu, mn >> 16);
-
-        // ---- exact path for threads holding an edge vector or a non-finite key
-        if (edge || tmax >= kKeyPosInf || tmin <= kKeyNegInf) {
-            uint32_t tflags = 0;
-            tmax = 0;
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i) {
-                const int32_t v = cbeg + i * kThreads + tid;
-                if (v >= cend) continue;
-                const bool full = v >= vfull0 && v < vfull1;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    uint32_t out = 0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int32_t c = v * 8 + 2 * w + h - m;
-                        uint32_t key;
-                        if (full) {
-                            key = h ? (kv[i][w] >> 16) : (kv[i][w] & 0xFFFFu);
-                        } else if (c >= 0 && c < cols) {
-                            key = key_from_raw(h ? (kv[i][w] >> 16) : (kv[i][w] & 0xFFFFu));
-                        } else {
-                            continue; // outside the row: key 0, never a candidate, no flag
-                        }
-                        if (key > kKeyPosInf || key < kKeyNegInf) {
-                            tflags |= 1u; // NaN
-                            key = 0;
-                        } else if (key == kKeyPosInf) {
-                            tflags |= 2u;
-                        } else if (key == kKeyNegInf) {
-                            tflags |= 4u;
-                        }
-                        tmax = max(tmax, key);
-                        out |= key << (16 * h);
-                    }
-                    kv[i][w] = out;
-                }
-            }
-            if (tflags) atomicOr(&sm.flags, tflags);
-        }
-
-        // ---- prefilter threshold: min over warps of the warp's j-th largest thread max
-        {
-            uint32_t v = tmax, cnt = 0, tw = 0;
-            for (int it = 0; it < j; ++it) {
-                const uint32_t mval = __reduce_max_sync(0xFFFFFFFFu, v);
-                if (mval == 0) break;
-                cnt += __popc(__ballot_sync(0xFFFFFFFFu, v == mval));
-                if (cnt >= (uint32_t)j) {
-                    tw = mval;
-                    break;
-                }
-                if (v == mval) v = 0;
-            }
-            if ((tid & 31) == 0) sm.warp_t[tid >> 5] = tw;
-        }
-        if (tid == 0) sm.n_cand = 0;
-        __syncthreads();
-        uint32_t t0 = 0xFFFFu;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
-        uint32_t t_floor = max(key_floor(t0), 1u);
-        const int run_len = sm.run_len;
-        if (run_len == k) {
-            // a new entry must beat the running k-th strictly (it has a higher column)
-            const uint32_t kth = (uint32_t)(sm.list[run_i][k - 1] >> 48);
-            t_floor = max(t_floor, kth + 1);
-        }
-
-        // ---- candidates
-        if (t_floor <= 0xFFFFu) {
-            const uint32_t tm1 = (t_floor - 1) * 0x10001u;
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i)
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t key2 = kv[i][w];
-                    if (max_u16x2(key2, tm1) != tm1) {
-                        const int local = (i * kThreads + tid) * 8 + 2 * w;
-                        if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local);
-                        if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1);
-                    }
-                }
-        }
-        __syncthreads();
-        uint32_t n = sm.n_cand;
-        if (n > (uint32_t)kCandCap) {
-            // stage the chunk's keys in column order; what is below t_floor is
-            // not a candidate and becomes 0
-            const uint32_t f = t_floor;
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i) {
-                uint4 q;
-                uint32_t *qw = &q.x;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint32_t lo = kv[i][w] & 0xFFFFu, hi = kv[i][w] >> 16;
-                    qw[w] = (lo >= f ? lo : 0u) | ((hi >= f ? hi : 0u) << 16);
-                }
-                reinterpret_cast<uint4 *>(sm.keys)[i * kThreads + tid] = q;
-            }
-            __syncthreads();
-            exact_select(t_floor, k, sm);
-            n = sm.n_cand; // == k
-        }
-        if (tid >= (int)n && tid < (int)((n + 3) & ~3u)) sm.cand[tid] = 0;
-        __syncthreads();
-
-        // ---- rank the candidates: rank = number of larger composites
-        if (tid < (int)n) {
-            const uint32_t e = sm.cand[tid];
-            uint32_t rank = 0;
-            const uint4 *c4 = reinterpret_cast<const uint4 *>(sm.cand);
-            for (uint32_t u = 0; u < (n + 3) >> 2; ++u) {
-                const uint4 q = c4[u];
-                rank += (q.x > e) + (q.y > e) + (q.z > e) + (q.w > e);
-            }
-            if (rank < (uint32_t)k) sm.list[chunk_i][rank] = entry_from_cand(e, sm.cand_raw[tid], col_base);
-        }
-        __syncthreads();
-        const int chunk_len = min((int)n, k);
-        if (run_len == 0) {
-            const int t = run_i;
-            run_i = chunk_i;
-            chunk_i = t;
-        } else if (chunk_len > 0) {
-            merge_lists(sm.list[run_i], run_len, sm.list[chunk_i], chunk_len, sm.list[free_i], k);
-            const int t = run_i;
-            run_i = free_i;
-            free_i = t;
-        }
-        __syncthreads();
-        if (tid == 0) sm.run_len = min(k, run_len + chunk_len);
-        __syncthreads();
+        const uint32_t tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+        select_chunk(kv, tmax, nvalid, col_base, k, sm, keys, run_i, chunk_i, free_i, run_len);
+        __syncthreads(); // the running list is read by the next chunk's threshold
     }
 
-    const uint64_t *final_list;
-    int final_len;
-    uint32_t flags;
-    if constexpr (S == 1) {
-        final_list = sm.list[run_i];
-        final_len = sm.run_len;
-        flags = sm.flags;
-    } else {
-        // ---- push this span's list into the leader's shared memory
-        asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); // every CTA has started
-        cg::cluster_group cluster = cg::this_cluster();
-        uint64_t *g = cluster.map_shared_rank(&sm.gather[span][0], 0);
-        const int len = sm.run_len;
-        for (int t = tid; t < len; t += kThreads) g[t] = sm.list[run_i][t];
-        if (tid == 0) {
-            *cluster.map_shared_rank(&sm.glen[span], 0) = len;
-            *cluster.map_shared_rank(&sm.gflags[span], 0) = sm.flags;
-        }
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        if (span != 0) return;
-
-        // ---- leader: pairwise merge tree over the S lists
-        uint64_t(*src)[kMaxK] = sm.gather;
-        uint64_t(*dst)[kMaxK] = sm.gather2;
-        int32_t *src_len = sm.glen;
-        int32_t *dst_len = sm.glen2;
-        flags = 0;
-#pragma unroll
-        for (int s = 0; s < S; ++s) flags |= sm.gflags[s];
-        for (int nl = S; nl > 1; nl >>= 1) {
-            for (int t = tid; t < nl * kMaxK; t += kThreads) {
-                const int l = t / kMaxK, pos = t % kMaxK;
-                if (pos >= src_len[l]) continue;
-                const uint64_t x = src[l][pos];
-                const int p = l ^ 1;
-                const int out = pos + count_greater(src[p], src_len[p], x);
-                if (out < k) dst[l >> 1][out] = x;
-            }
-            if (tid < nl / 2) dst_len[tid] = min(k, src_len[2 * tid] + src_len[2 * tid + 1]);
-            __syncthreads();
-            // swap roles: the next level reads what this one wrote
-            uint64_t(*tl)[kMaxK] = src;
-            src = dst;
-            dst = tl;
-            int32_t *tlen = src_len;
-            src_len = dst_len;
-            dst_len = tlen;
-        }
-        final_list = src[0];
-        final_len = src_len[0];
-    }
-
-    // ---- write the row
-    for (int t = tid; t < k; t += kThreads) {
-        const int64_t o = row * k + t;
-        if (t < final_len) {
-            const uint64_t e = final_list[t];
-            out_idx[o] = entry_col(e);
-            out_val[o] = (uint16_t)(e & 0xFFFFu);
-        } else {
-            out_idx[o] = -1;
-            out_val[o] = (uint16_t)kEmptyVal;
-        }
-    }
+    // ---- push this span's list into the leader's shared memory
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); // every CTA has started
+    cg::cluster_group cluster = cg::this_cluster();
+    uint64_t *gl = cluster.map_shared_rank(&sg.gather[span][0], 0);
+    const int len = run_len;
+    for (int t = tid; t < len; t += kThreads) gl[t] = sm.list[run_i][t];
     if (tid == 0) {
-        out_count[row] = final_len;
-        out_mask[row] = flags;
+        *cluster.map_shared_rank(&sg.glen[span], 0) = len;
+        *cluster.map_shared_rank(&sg.gflags[span], 0) = sm.flags;
     }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    if (span != 0) return;
+
+    // ---- leader: pairwise merge tree over the S lists, then the row
+    uint32_t flags = 0;
+#pragma unroll
+    for (int s = 0; s < S; ++s) flags |= sg.gflags[s];
+    int flen = 0;
+    const uint64_t *fin = merge_tree(sg, S, k, flen);
+    write_row(row, fin, flen, flags, k, out_idx, out_val, out_count, out_mask);
 }
 
 // ---------------------------------------------------------------- host side
+
+constexpr size_t kStreamSmemBytes = (size_t)kStages * kChunkVecs * 16 + sizeof(SmemCore);
 
 struct DeviceInfo {
     bool ready = false;
@@ -630,8 +969,9 @@ int fail_cuda(cudaError_t e)
     return TF_TOPK_ERR_CUDA;
 }
 
-// Per-device set-up, once: check the architecture, allow the 16-CTA cluster.
-int device_setup(int *sm_count)
+// Per-device set-up, once: check the architecture, allow the 16-CTA cluster and
+// the stream kernel's shared-memory ring.
+int device_setup(int *dev_out, int *sm_count)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -648,15 +988,76 @@ int device_setup(int *sm_count)
         if (major != 10 || minor != 3) {
             d.status = TF_TOPK_ERR_DEVICE;
         } else {
-            e = cudaFuncSetAttribute(topk_rows_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kStreamSmemBytes);
             if (e != cudaSuccess) return fail_cuda(e);
             d.status = TF_TOPK_OK;
         }
         d.sm_count = sms;
         d.ready = true;
     }
+    *dev_out = dev;
     *sm_count = d.sm_count;
     return d.status;
+}
+
+// Scratch of the stream kernel: two partial lists and one ticket per CTA.
+// One area per (device, stream) so that calls on different streams never share
+// it; calls on one stream are ordered by the stream.  Tickets start at zero and
+// every merge puts its ticket back to zero.
+struct Scratch {
+    uint64_t *partials = nullptr;
+    uint32_t *tickets = nullptr;
+    int64_t ctas = 0;
+};
+
+struct ScratchKey {
+    int dev;
+    cudaStream_t stream;
+    std::thread::id thread; // only set for the per-thread default stream
+    bool operator<(const ScratchKey &o) const
+    {
+        if (dev != o.dev) return dev < o.dev;
+        if (stream != o.stream) return stream < o.stream;
+        return thread < o.thread;
+    }
+};
+
+std::mutex g_scratch_mutex;
+std::map<ScratchKey, Scratch> g_scratch;
+
+size_t partial_bytes(int64_t ctas) { return (size_t)ctas * 2 * (kMaxK + 1) * sizeof(uint64_t); }
+
+int get_scratch(int dev, cudaStream_t stream, int64_t ctas, Scratch **out)
+{
+    ScratchKey key{dev, stream, std::thread::id()};
+    if (stream == cudaStreamPerThread) key.thread = std::this_thread::get_id();
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    Scratch &s = g_scratch[key];
+    if (s.ctas < ctas) {
+        if (s.partials) {
+            // the old area may still be in use by work queued on this stream
+            cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return fail_cuda(e);
+            cudaFree(s.partials);
+            cudaFree(s.tickets);
+            s = Scratch();
+        }
+        cudaError_t e = cudaMalloc(&s.partials, partial_bytes(ctas));
+        if (e == cudaSuccess) e = cudaMalloc(&s.tickets, (size_t)ctas * sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaMemsetAsync(s.tickets, 0, (size_t)ctas * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) {
+            cudaFree(s.partials);
+            cudaFree(s.tickets);
+            s = Scratch();
+            return fail_cuda(e);
+        }
+        s.ctas = ctas;
+    }
+    *out = &s;
+    return TF_TOPK_OK;
 }
 
 int validate(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
@@ -676,24 +1077,42 @@ int validate(const void *logits, int64_t rows, int64_t cols, int64_t row_stride,
     return TF_TOPK_OK;
 }
 
-// Span count for a shape: rows below 4096 columns stay on one CTA (the pages'
-// threshold); wider rows use enough spans that each CTA holds at most one
-// chunk, and more while the grid is small next to the SM count.
-int32_t pick_spans(int64_t rows, int64_t cols, int sm_count)
+// Vectors per row in the stream kernel's rows x vectors space: enough for any
+// alignment of the row start.
+int32_t vectors_per_row(int64_t cols) { return (int32_t)((cols + 14) >> 3); }
+
+// Stream-plan geometry: the range each CTA gets, and the CTA count.
+void stream_geometry(int64_t rows, int64_t cols, int sm_count, bool one_row_per_cta, int64_t *per_out,
+                     int64_t *ctas_out)
 {
-    if (cols < 4096) return 1;
-    const int64_t nvec = (cols + 7) / 8 + 1;
-    int32_t s = 1;
-    while (s < kMaxSpans && (nvec + s - 1) / s > kChunkVecs) s <<= 1;
-    while (s < kMaxSpans && rows * s < 2LL * sm_count && (nvec + 2 * s - 1) / (2 * s) >= 2 * kThreads)
-        s <<= 1;
-    return s;
+    const int64_t nvr = vectors_per_row(cols);
+    const int64_t total = rows * nvr;
+    int64_t per;
+    if (one_row_per_cta) {
+        per = nvr;
+    } else {
+        const int64_t slots = (int64_t)sm_count * kStreamCtasPerSm;
+        per = (total + slots - 1) / slots;
+        per = per < kMinVecsPerCta ? kMinVecsPerCta : per;
+        const int64_t min_piece = (nvr + kMaxPieces - 2) / (kMaxPieces - 1); // a row meets <= kMaxPieces CTAs
+        per = per < min_piece ? min_piece : per;
+    }
+    *per_out = per;
+    *ctas_out = (total + per - 1) / per;
+}
+
+int32_t pick_plan(int64_t rows, int64_t cols, int sm_count)
+{
+    (void)rows;
+    (void)cols;
+    (void)sm_count;
+    return TF_TOPK_PLAN_STREAM;
 }
 
 template <int S>
-cudaError_t launch(const uint16_t *logits, int64_t rows, int32_t cols, int64_t row_stride, int32_t k,
-                   int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_mask,
-                   cudaStream_t stream)
+cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, int64_t row_stride, int32_t k,
+                           int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_mask,
+                           cudaStream_t stream)
 {
     const int64_t max_rows = (int64_t)INT32_MAX / S;
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
@@ -704,15 +1123,13 @@ cudaError_t launch(const uint16_t *logits, int64_t rows, int32_t cols, int64_t r
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
-        if (S > 1) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = S;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-        }
-        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_rows_kernel<S>, logits + r0 * row_stride, cols,
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<S>, logits + r0 * row_stride, cols,
                                            row_stride, k, out_idx + r0 * k, out_val + r0 * k,
                                            out_count + r0, out_mask + r0);
         if (e != cudaSuccess) return e;
@@ -720,28 +1137,72 @@ cudaError_t launch(const uint16_t *logits, int64_t rows, int32_t cols, int64_t r
     return cudaSuccess;
 }
 
+int launch_stream(int dev, int sm_count, const uint16_t *logits, int64_t rows, int64_t cols,
+                  int64_t row_stride, int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                  uint32_t *out_mask, bool one_row_per_cta, cudaStream_t stream)
+{
+    const int32_t nvr = vectors_per_row(cols);
+    // one launch covers at most 2^31-1 CTAs; longer matrices go in row blocks
+    const int64_t rows_per_launch = one_row_per_cta ? (int64_t)INT32_MAX : rows;
+    for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
+        const int64_t nr = rows - r0 < rows_per_launch ? rows - r0 : rows_per_launch;
+        int64_t per = 0, ctas = 0;
+        stream_geometry(nr, cols, sm_count, one_row_per_cta, &per, &ctas);
+        uint64_t *partials = nullptr;
+        uint32_t *tickets = nullptr;
+        if (!one_row_per_cta) {
+            Scratch *s = nullptr;
+            const int st = get_scratch(dev, stream, ctas, &s);
+            if (st != TF_TOPK_OK) return st;
+            partials = s->partials;
+            tickets = s->tickets;
+        }
+        topk_stream_kernel<<<(unsigned)ctas, kThreads, kStreamSmemBytes, stream>>>(
+            logits + r0 * row_stride, (int32_t)cols, row_stride, k, nvr, nr * nvr, per, out_idx + r0 * k,
+            out_val + r0 * k, out_count + r0, out_mask + r0, partials, tickets);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TF_TOPK_OK;
+}
+
 int run(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k, int32_t *out_idx,
-        uint16_t *out_val, int32_t *out_count, uint32_t *out_mask, int32_t spans, void *stream)
+        uint16_t *out_val, int32_t *out_count, uint32_t *out_mask, int32_t plan, void *stream)
 {
     int st = validate(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask);
     if (st != TF_TOPK_OK) return st;
-    if (spans != 0 && spans != 1 && spans != 2 && spans != 4 && spans != 8 && spans != 16)
-        return TF_TOPK_ERR_SPANS;
+    if (plan != TF_TOPK_PLAN_AUTO && plan != TF_TOPK_PLAN_SINGLE && plan != TF_TOPK_PLAN_CLUSTER2 &&
+        plan != TF_TOPK_PLAN_CLUSTER4 && plan != TF_TOPK_PLAN_CLUSTER8 && plan != TF_TOPK_PLAN_CLUSTER16 &&
+        plan != TF_TOPK_PLAN_STREAM)
+        return TF_TOPK_ERR_PLAN;
     if (rows == 0) return TF_TOPK_OK;
-    int sm_count = 0;
-    st = device_setup(&sm_count);
+    int dev = 0, sm_count = 0;
+    st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return st;
-    if (spans == 0) spans = pick_spans(rows, cols, sm_count);
+    if (plan == TF_TOPK_PLAN_AUTO) plan = pick_plan(rows, cols, sm_count);
     const uint16_t *x = static_cast<const uint16_t *>(logits);
     const int32_t c = (int32_t)cols;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (spans) {
-    case 1: e = launch<1>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s); break;
-    case 2: e = launch<2>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s); break;
-    case 4: e = launch<4>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s); break;
-    case 8: e = launch<8>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s); break;
-    default: e = launch<16>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s); break;
+    cudaError_t e = cudaSuccess;
+    switch (plan) {
+    case TF_TOPK_PLAN_SINGLE:
+        return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
+                             true, s);
+    case TF_TOPK_PLAN_STREAM:
+        return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
+                             false, s);
+    case TF_TOPK_PLAN_CLUSTER2:
+        e = launch_cluster<2>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        break;
+    case TF_TOPK_PLAN_CLUSTER4:
+        e = launch_cluster<4>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        break;
+    case TF_TOPK_PLAN_CLUSTER8:
+        e = launch_cluster<8>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        break;
+    default:
+        e = launch_cluster<16>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        break;
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
@@ -756,15 +1217,15 @@ int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_str
                  int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask,
                  void *stream)
 {
-    return run(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask, 0,
-               stream);
+    return run(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask,
+               TF_TOPK_PLAN_AUTO, stream);
 }
 
-int tf_topk_bf16_spans(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
-                       int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
-                       uint32_t *out_nonfinite_mask, int32_t spans, void *stream)
+int tf_topk_bf16_with_plan(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                           int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                           uint32_t *out_nonfinite_mask, int32_t plan, void *stream)
 {
-    return run(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask, spans,
+    return run(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask, plan,
                stream);
 }
 
@@ -772,10 +1233,32 @@ int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)
 {
     if (k < 1 || k > kMaxK) return -TF_TOPK_ERR_K;
     if (rows < 0 || cols < 1 || cols > (int64_t)INT32_MAX - 64) return -TF_TOPK_ERR_SHAPE;
-    int sm_count = 0;
-    const int st = device_setup(&sm_count);
+    int dev = 0, sm_count = 0;
+    const int st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return -st;
-    return pick_spans(rows, cols, sm_count);
+    return pick_plan(rows, cols, sm_count);
+}
+
+int tf_topk_device_fault(void)
+{
+    uint32_t f = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&f, g_fault, sizeof f);
+    if (e != cudaSuccess) return -fail_cuda(e);
+    if (f != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_fault, &zero, sizeof zero);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        // a CTA that gave up may have left a ticket half-counted: reset them all
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        int dev = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        for (auto &kv : g_scratch)
+            if (e == cudaSuccess && kv.first.dev == dev && kv.second.tickets)
+                e = cudaMemset(kv.second.tickets, 0, (size_t)kv.second.ctas * sizeof(uint32_t));
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return -fail_cuda(e);
+    }
+    return (int)f;
 }
 
 int32_t tf_topk_bf16_max_k(void) { return kMaxK; }
@@ -791,7 +1274,7 @@ const char *tf_topk_strerror(int status)
     case TF_TOPK_ERR_SHAPE: return "invalid shape (rows, cols or row_stride)";
     case TF_TOPK_ERR_K: return "k out of range (1..TF_TOPK_MAX_K)";
     case TF_TOPK_ERR_ALIGN: return "misaligned pointer";
-    case TF_TOPK_ERR_SPANS: return "spans must be 0, 1, 2, 4, 8 or 16";
+    case TF_TOPK_ERR_PLAN: return "unknown plan code";
     case TF_TOPK_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
     case TF_TOPK_ERR_CUDA: return "CUDA runtime error (see tf_topk_last_cuda_error)";
     default: return "unknown status";

@@ -13,7 +13,12 @@ PKG = Path(__file__).resolve().parent
 LIBRARY = PKG / "libtf_topk.so"
 
 # status codes (include/tf_topk.h)
-OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_SPANS, ERR_DEVICE, ERR_CUDA = range(8)
+OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_PLAN, ERR_DEVICE, ERR_CUDA = range(8)
+
+# launch plans (include/tf_topk.h)
+PLAN_AUTO, PLAN_SINGLE, PLAN_STREAM = 0, 1, 32
+PLAN_CLUSTER = {2: 2, 4: 4, 8: 8, 16: 16}
+PLANS = (PLAN_AUTO, PLAN_SINGLE, 2, 4, 8, 16, PLAN_STREAM)
 
 _lib = None
 
@@ -35,9 +40,11 @@ def library() -> ctypes.CDLL:
         c_i64, c_i32, c_p = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
         lib.tf_topk_bf16.restype = ctypes.c_int
         lib.tf_topk_bf16.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
-        lib.tf_topk_bf16_spans.restype = ctypes.c_int
-        lib.tf_topk_bf16_spans.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p,
-                                           c_i32, c_p]
+        lib.tf_topk_bf16_with_plan.restype = ctypes.c_int
+        lib.tf_topk_bf16_with_plan.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p,
+                                               c_p, c_i32, c_p]
+        lib.tf_topk_device_fault.restype = ctypes.c_int
+        lib.tf_topk_device_fault.argtypes = []
         lib.tf_topk_bf16_plan.restype = c_i32
         lib.tf_topk_bf16_plan.argtypes = [c_i64, c_i64, c_i32]
         for name in ("tf_topk_bf16_max_k", "tf_topk_bf16_max_spans", "tf_topk_bf16_cta_threads",
@@ -84,23 +91,31 @@ def tf_topk_bf16(logits: int, rows: int, cols: int, row_stride: int, k: int, out
                                   out_nonfinite_mask, stream)
 
 
-def tf_topk_bf16_spans(logits: int, rows: int, cols: int, row_stride: int, k: int, out_idx: int,
-                       out_val: int, out_count: int, out_nonfinite_mask: int, spans: int,
-                       stream: int | None) -> int:
-    """The C entry point with an explicit span count; returns the status code."""
-    return library().tf_topk_bf16_spans(logits, rows, cols, row_stride, k, out_idx, out_val,
-                                        out_count, out_nonfinite_mask, spans, stream)
+def tf_topk_bf16_with_plan(logits: int, rows: int, cols: int, row_stride: int, k: int,
+                           out_idx: int, out_val: int, out_count: int, out_nonfinite_mask: int,
+                           plan: int, stream: int | None) -> int:
+    """The C entry point with an explicit launch plan; returns the status code."""
+    return library().tf_topk_bf16_with_plan(logits, rows, cols, row_stride, k, out_idx, out_val,
+                                            out_count, out_nonfinite_mask, plan, stream)
+
+
+def device_fault() -> int:
+    """0, or the fault code a kernel recorded since the last check (then cleared)."""
+    r = library().tf_topk_device_fault()
+    if r < 0:
+        _check(-r)
+    return r
 
 
 def plan(rows: int, cols: int, k: int) -> int:
-    """Span count the library picks for a shape on the current device."""
+    """Launch plan (TF_TOPK_PLAN_* code) the library picks for a shape on the current device."""
     r = library().tf_topk_bf16_plan(rows, cols, k)
     if r < 0:
         _check(-r)
     return r
 
 
-def topk_bf16(x, k: int, *, spans: int = 0, out=None, stream=None):
+def topk_bf16(x, k: int, *, plan: int = 0, out=None, stream=None):
     """Exact top-k of every row of a CUDA bf16 matrix.
 
     ``x``: a CUDA tensor of dtype bfloat16 (or int16/uint16 holding bf16 bits),
@@ -109,7 +124,9 @@ def topk_bf16(x, k: int, *, spans: int = 0, out=None, stream=None):
     Returns ``(idx int32[rows,k], val bfloat16[rows,k], count int32[rows],
     mask int32[rows])``; ``mask`` holds the uint32 bits (1 NaN, 2 +inf, 4 -inf).
     ``out`` may supply those four tensors.  Runs on ``stream`` (a
-    ``torch.cuda.Stream``) or the current stream of ``x``'s device.
+    ``torch.cuda.Stream``) or the current stream of ``x``'s device.  ``plan``
+    picks the launch plan (``PLANS``; 0 = the library's choice); every plan
+    gives the same result.
     """
     import torch
 
@@ -144,8 +161,8 @@ def topk_bf16(x, k: int, *, spans: int = 0, out=None, stream=None):
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     with torch.cuda.device(dev):
-        status = tf_topk_bf16_spans(x.data_ptr(), rows, cols, row_stride, k, idx.data_ptr(),
-                                    val.data_ptr(), count.data_ptr(), mask.data_ptr(), spans,
-                                    stream.cuda_stream)
+        status = tf_topk_bf16_with_plan(x.data_ptr(), rows, cols, row_stride, k, idx.data_ptr(),
+                                        val.data_ptr(), count.data_ptr(), mask.data_ptr(), plan,
+                                        stream.cuda_stream)
     _check(status)
     return idx, val, count, mask
