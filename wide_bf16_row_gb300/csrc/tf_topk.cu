@@ -29,12 +29,12 @@
 //     absorbs the chunks of a row piece; pieces are merged pairwise (the
 //     pages' tournament) in the same order.
 //
-// Kernel 1, topk_stream_kernel (the default plan): a persistent grid of two
-// CTAs per SM.  The rows x vectors space is cut into equal contiguous ranges,
-// one per CTA, so every SM gets the same number of bytes whatever the shape.
-// Each CTA streams its range through a 3-stage shared-memory ring filled by
-// TMA bulk copies (cp.async.bulk + mbarrier): two chunks are in flight while
-// one is selected.  A row cut by a range boundary leaves one partial list per
+// Kernel 1, topk_stream_kernel (the default plan): a persistent grid of
+// kStreamCtasPerSm CTAs per SM.  The rows x vectors space is cut into equal
+// contiguous ranges, one per CTA, so every SM gets the same number of bytes
+// whatever the shape.  Each CTA streams its range through a kStages-deep
+// shared-memory ring filled by TMA bulk copies (cp.async.bulk + mbarrier): the
+// next chunk is in flight while one is selected.  A row cut by a range boundary leaves one partial list per
 // piece in a small scratch area; the last CTA to finish a piece of that row
 // (an atomic ticket) merges them and writes the row.  With one range per row
 // the same kernel is the single-CTA control path.
@@ -72,8 +72,8 @@ constexpr int kChunkCols = kChunkVecs * 8;           // 16384 columns
 constexpr int kMaxK = TF_TOPK_MAX_K;
 constexpr int kMaxSpans = TF_TOPK_MAX_SPANS;
 constexpr int kCandCap = 256;        // candidates ranked directly (one per thread)
-constexpr int kStages = 3;           // TMA ring depth of the stream kernel
-constexpr int kStreamCtasPerSm = 2;  // resident stream CTAs per SM
+constexpr int kStages = 2;           // TMA ring depth of the stream kernel
+constexpr int kStreamCtasPerSm = 3;  // resident stream CTAs per SM
 constexpr int kMinVecsPerCta = 1024; // smallest range a stream CTA is given
 constexpr int kMaxPieces = kMaxSpans;// most pieces a stream row is cut into
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -87,6 +87,7 @@ static_assert((kMaxK + kWarps - 1) / kWarps <= 32, "per-warp order statistic nee
 static_assert(kMaxSpans == 16 && (kMaxSpans & (kMaxSpans - 1)) == 0, "merge tree over 2^n lists");
 static_assert(kMaxK == 64, "header and kernels agree on max_k");
 static_assert(kStages >= 2, "a ring needs two stages");
+static_assert(kVecPerThread * 4 == 32, "the candidate scan maps a lane to one word of a thread's slice");
 
 constexpr uint32_t kEmptyVal = 0x7FC0;
 constexpr uint32_t kKeyPosInf = 0xFF80;
@@ -459,14 +460,19 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    // ---- prefilter threshold.  The fw warps whose 32 lanes all hold data each
-    //      find the j-th largest of their lanes' maxima, j = ceil(k / fw); the
-    //      minimum t0 over them is reached by at least fw * j >= k elements.
-    //      With no such bound (a tiny chunk, or a warp without j positive
-    //      maxima) t0 = 0 and every element is a candidate.
-    const int fw = min(nvalid, kThreads) / 32;
-    const int j = fw ? (k + fw - 1) / fw : 33;
-    {
+    uint32_t t_floor;
+    if (run_len == k) {
+        // steady state: a new entry must beat the running k-th strictly (every
+        // column of this chunk is higher), and that bound needs no barrier
+        t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
+    } else {
+        // ---- prefilter threshold.  The fw warps whose 32 lanes all hold data
+        //      each find the j-th largest of their lanes' maxima, j = ceil(k / fw);
+        //      the minimum t0 over them is reached by at least fw * j >= k
+        //      elements.  With no such bound (a tiny chunk, or a warp without j
+        //      positive maxima) t0 = 0 and every element is a candidate.
+        const int fw = min(nvalid, kThreads) / 32;
+        const int j = fw ? (k + fw - 1) / fw : 33;
         uint32_t tw = 0xFFFFu; // warps without a full set of lanes do not bound
         if (warp < fw) {
             tw = 0;
@@ -485,17 +491,12 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
             }
         }
         if (lane == 0) sm.warp_t[warp] = tw;
-    }
-    if (tid == 0) sm.n_cand = 0;
-    __syncthreads();
-    uint32_t t0 = (fw == 0 || j > 32) ? 0u : 0xFFFFu;
+        __syncthreads();
+        uint32_t t0 = (fw == 0 || j > 32) ? 0u : 0xFFFFu;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
-    uint32_t t_floor = max(key_floor(t0), 1u);
-    if (run_len == k) {
-        // a new entry must beat the running k-th strictly (it has a higher column)
-        const uint32_t kth = (uint32_t)(sm.list[run_i][k - 1] >> 48);
-        t_floor = max(t_floor, kth + 1);
+        for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
+        t_floor = max(key_floor(t0), 1u);
+        if (run_len > 0 && run_len == k) t_floor = max(t_floor, (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u);
     }
 
     // ---- candidates: only threads whose max reaches t_floor hold any; each
@@ -515,8 +516,12 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
         if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local);
         if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1);
     }
+    // this thread's stage slots may have been written (exact key pass, spill);
+    // the stage is next written by a bulk copy (async proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     uint32_t n = sm.n_cand;
+    if (n == 0) return; // nothing reaches the threshold: the running list stands
     if (n > (uint32_t)kCandCap) {
         // heavy ties: stage every key in column order (below t_floor -> 0) and
         // select exactly
@@ -530,12 +535,11 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
             }
             stage[i * kThreads + tid] = make_uint4(q[0], q[1], q[2], q[3]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
         n = sm.n_cand; // == k
     }
-    // the stage may next be written by a bulk copy (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 
     // ---- rank the candidates: rank = number of larger composites
     if (tid < (int)n) {
@@ -551,6 +555,7 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
         if (rank < (uint32_t)k) sm.list[chunk_i][rank] = entry_from_cand(e, sm.cand_raw[tid], col_base);
     }
     __syncthreads();
+    if (tid == 0) sm.n_cand = 0; // every thread has read n; the next chunk pushes from 0
     const int chunk_len = min((int)n, k);
     if (run_len == 0) {
         const int t = run_i;
@@ -684,6 +689,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&sm.mbar[s], 1);
+        sm.n_cand = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -896,7 +902,10 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     const int32_t v_begin = min(nvec, span * per_span);
     const int32_t v_end = min(nvec, v_begin + per_span);
 
-    if (tid == 0) sm.flags = 0;
+    if (tid == 0) {
+        sm.flags = 0;
+        sm.n_cand = 0;
+    }
     __syncthreads();
     int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
 
