@@ -85,6 +85,10 @@ def _tie_rows(cols: int, seed: int) -> np.ndarray:
     mostly_nan[rng.choice(cols, size=min(cols, 10), replace=False)] = 0x8000
     rows.append(mostly_nan)
     rows.append(np.full(cols, 0xFFC1, np.uint16))                                    # all -NaN
+    asc = np.sort(synth.bf16_to_float(synth.round_to_bf16(                          # ascending: every
+        rng.standard_normal(cols).astype(np.float32))))                              # chunk beats the last
+    rows.append(synth.round_to_bf16(asc))
+    rows.append(synth.round_to_bf16(asc[::-1].copy()))                               # descending
     return np.stack(rows)
 
 

@@ -77,6 +77,8 @@ constexpr int kStreamCtasPerSm = 3;  // resident stream CTAs per SM
 constexpr int kMinVecsPerCta = 1024; // smallest range a stream CTA is given
 constexpr int kMaxPieces = kMaxSpans;// most pieces a stream row is cut into
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kPendCap = 512;        // stream kernel: candidates waiting for a merge
+constexpr int kMergeAt = 64;         // merge the waiting candidates once this many
 
 // The constant ties the pages ask for: a change to one of these fails the build.
 static_assert(kThreads % 32 == 0 && kThreads >= 64, "whole warps");
@@ -108,6 +110,7 @@ struct __align__(16) SmemCore {
     uint32_t scan[kWarps][4];
     uint64_t mbar[kStages];
     uint32_t n_cand;
+    uint32_t npend;                         // stream kernel: entries waiting in pend
     uint32_t flags;
     uint32_t kmax;
     uint32_t ticket;
@@ -188,6 +191,12 @@ __device__ __forceinline__ uint64_t entry_from_cand(uint32_t c32, uint32_t raw, 
 __device__ __forceinline__ int32_t entry_col(uint64_t e)
 {
     return (int32_t)(~(uint32_t)(e >> 16));
+}
+
+// The list entry of key `key` (order-preserving, not 0) at row column `col`.
+__device__ __forceinline__ uint64_t list_entry(uint32_t key, int32_t col)
+{
+    return ((uint64_t)canon(key) << 48) | ((uint64_t)(~(uint32_t)col) << 16) | (uint64_t)raw_from_key(key);
 }
 
 // Number of entries of a descending list of distinct values that exceed x.
@@ -571,6 +580,72 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
     // the next reader of the running list is behind a barrier of the caller
 }
 
+
+// Stream kernel, steady state: the running list (list[run_i], run_len
+// entries, descending) absorbs the np pending entries pend[0..np) (distinct,
+// any order) into list[out_i]; the indices swap and the pending count is
+// cleared.  A rank merge: an entry's place is the number of larger pending
+// entries plus the number of larger running entries.  Block-uniform.
+__device__ __noinline__ void merge_pending(SmemCore &sm, const uint64_t *pend, int np, int k, int &run_i,
+                                           int &out_i, int &run_len)
+{
+    const int tid = threadIdx.x;
+    const uint64_t *run = sm.list[run_i];
+    uint64_t *out = sm.list[out_i];
+    const int total = np + run_len;
+    for (int t = tid; t < total; t += kThreads) {
+        const uint64_t x = t < np ? pend[t] : run[t - np];
+        uint32_t g = 0;
+        int u = 0;
+        for (; u + 1 < np; u += 2) {
+            const ulonglong2 p2 = *reinterpret_cast<const ulonglong2 *>(pend + u);
+            g += (p2.x > x) + (p2.y > x);
+        }
+        if (u < np) g += pend[u] > x;
+        if (t < np) {
+            const int pos = (int)g + count_greater(run, run_len, x);
+            if (pos < k) out[pos] = x;
+        } else if ((t - np) + (int)g < k) {
+            out[(t - np) + g] = x;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) sm.npend = 0;
+    const int t = run_i;
+    run_i = out_i;
+    out_i = t;
+    run_len = min(k, run_len + np);
+    __syncthreads();
+}
+
+// Stream kernel, steady state: a chunk whose candidates overflowed the pending
+// buffer.  Its keys are still in its stage (written back there, 0 where
+// nothing may be selected); select its best k exactly over the keys that reach
+// t_floor and put them into pend[np_before..np_before + k).  Returns the new
+// pending count.  Block-uniform.
+__device__ __noinline__ int lazy_overflow(SmemCore &sm, uint64_t *pend, uint4 *stage, uint32_t t_floor,
+                                          int32_t col_base, int np_before, int k)
+{
+    const int tid = threadIdx.x;
+    for (int i = 0; i < kVecPerThread; ++i) {
+        uint4 q = stage[i * kThreads + tid];
+        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
+            w[j] = (lo >= t_floor ? lo : 0u) | ((hi >= t_floor ? hi : 0u) << 16);
+        }
+        stage[i * kThreads + tid] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
+    const int n = (int)sm.n_cand; // == k
+    for (int t = tid; t < n; t += kThreads)
+        pend[np_before + t] = entry_from_cand(sm.cand[t], sm.cand_raw[t], col_base);
+    __syncthreads();
+    return np_before + n;
+}
+
 // Merge sm.gather[0..nl) (nl a power of two, lengths in sm.glen) pairwise into
 // one list; returns it (in sm.gather or sm.gather2) and its length.
 __device__ __forceinline__ const uint64_t *merge_tree(SmemGather &sm, int nl, int k, int &out_len)
@@ -727,27 +802,62 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
     if (tid == 0)
         for (int s = 0; s < kStages - 1; ++s) issue_next();
 
+    uint64_t *pend = reinterpret_cast<uint64_t *>(dsmem + (size_t)kStages * kChunkVecs * 16 + sizeof(SmemCore));
     int c = 0; // chunks consumed
     bool aborted = false;
     int64_t g = g0;
     int64_t row = row0; // the consumer's own cursor (thread 0's producer cursor runs ahead)
     int32_t vb = (int32_t)(g0 - row0 * nvr);
+    int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
     while (g < g1 && !aborted) {
         const int32_t ve = (int32_t)min((int64_t)nvr, (int64_t)vb + (g1 - g));
         const ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
-        if (tid == 0) sm.flags = 0;
-        int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
+        if (tid == 0) {
+            sm.flags = 0;
+            sm.npend = 0;
+        }
+        run_i = 0;
+        chunk_i = 1;
+        free_i = 2;
+        run_len = 0;
+        // the previous chunk, when it only pushed its candidates (steady state)
+        bool prev_lazy = false;
+        uint4 *prev_st = nullptr;
+        uint32_t prev_t = 0;
+        int32_t prev_col_base = 0;
+        int prev_np0 = 0;
+
+        // Pending candidates of the previous lazy chunk: an overflow is
+        // re-selected exactly from its stage (not yet refilled) and merged; a
+        // full enough buffer is merged.  `at_end`: merge whatever waits.
+        // Returns the pending count afterwards (the same in every thread).
+        auto settle = [&](bool at_end) -> int {
+            int np = (int)sm.npend;
+            bool force = at_end;
+            if (np > kPendCap) {
+                np = lazy_overflow(sm, pend, prev_st, prev_t, prev_col_base, prev_np0, k);
+                force = true;
+            }
+            if (np >= kMergeAt || (force && np > 0)) {
+                merge_pending(sm, pend, np, k, run_i, free_i, run_len);
+                np = 0;
+            }
+            return np;
+        };
+        int np_now = 0; // pending entries, as every thread knows them
 
         for (int32_t cb = vb; cb < ve; cb += kChunkVecs) {
             const int32_t ce = min(ve, cb + kChunkVecs);
             const int s = c % kStages;
             // one thread waits for the chunk's bulk copy; the barrier hands it on
+            // (and makes the previous chunk's pushes visible)
             bool ok = true;
             if (tid == 0) ok = mbar_wait(&sm.mbar[s], (uint32_t)((c / kStages) & 1));
             if (__syncthreads_or(!ok)) {
                 aborted = true;
                 break;
             }
+            if (prev_lazy) np_now = settle(false);
             if (tid == 0) {
                 // every thread is past the previous chunk: refill its stage
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -785,11 +895,49 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                 }
                 tmax = chunk_keys<false>(kv, nvalid, col_base, cols, st, sm);
             }
-            select_chunk(kv, tmax, nvalid, col_base, k, sm, st, run_i, chunk_i, free_i, run_len);
+            if (run_len < k) {
+                // the piece's first chunks: a prefilter bound and an immediate merge
+                select_chunk(kv, tmax, nvalid, col_base, k, sm, st, run_i, chunk_i, free_i, run_len);
+                prev_lazy = false;
+            } else {
+                // steady state: a new entry must beat the running k-th strictly
+                // (every column of this chunk is higher).  Candidates are rare; they
+                // go to the pending buffer as list entries, with no barrier.  The
+                // keys are written back over the stage in case the buffer overflows.
+                const uint32_t t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
+#pragma unroll
+                for (int i = 0; i < kVecPerThread; ++i)
+                    st[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+                __syncwarp();
+                const int lane = tid & 31, warp = tid >> 5;
+                for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, tmax >= t_floor); hits; hits &= hits - 1) {
+                    const int src = warp * 32 + __ffs(hits) - 1;
+                    const int lv = (lane >> 2) * kThreads + src;
+                    const uint32_t key2 = reinterpret_cast<const uint32_t *>(st)[lv * 4 + (lane & 3)];
+                    const int32_t col0 = col_base + lv * 8 + 2 * (lane & 3);
+                    const uint32_t klo = key2 & 0xFFFFu, khi = key2 >> 16;
+                    if (klo >= t_floor) {
+                        const uint32_t slot = atomicAdd(&sm.npend, 1u);
+                        if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(klo, col0);
+                    }
+                    if (khi >= t_floor) {
+                        const uint32_t slot = atomicAdd(&sm.npend, 1u);
+                        if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(khi, col0 + 1);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                prev_lazy = true;
+                prev_st = st;
+                prev_t = t_floor;
+                prev_col_base = col_base;
+                prev_np0 = np_now;
+            }
             ++c;
         }
         if (aborted) break;
-        __syncthreads(); // the running list is complete
+        __syncthreads(); // the running list, or the last chunk's pushes, are complete
+        if (prev_lazy) settle(true);
+        prev_lazy = false;
 
         // ---- end of a row piece
         const int len = run_len;
@@ -959,7 +1107,8 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
 
 // ---------------------------------------------------------------- host side
 
-constexpr size_t kStreamSmemBytes = (size_t)kStages * kChunkVecs * 16 + sizeof(SmemCore);
+constexpr size_t kStreamSmemBytes =
+    (size_t)kStages * kChunkVecs * 16 + sizeof(SmemCore) + (size_t)kPendCap * sizeof(uint64_t);
 
 struct DeviceInfo {
     bool ready = false;
