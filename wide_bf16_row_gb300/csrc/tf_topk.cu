@@ -72,8 +72,8 @@ constexpr int kChunkCols = kChunkVecs * 8;           // 16384 columns
 constexpr int kMaxK = TF_TOPK_MAX_K;
 constexpr int kMaxSpans = TF_TOPK_MAX_SPANS;
 constexpr int kCandCap = 256;        // candidates ranked directly (one per thread)
-constexpr int kStages = 2;           // TMA ring depth of the stream kernel
-constexpr int kStreamCtasPerSm = 3;  // resident stream CTAs per SM
+constexpr int kStages = 3;           // TMA ring depth of the stream kernel
+constexpr int kStreamCtasPerSm = 2;  // resident stream CTAs per SM
 constexpr int kMinVecsPerCta = 1024; // smallest range a stream CTA is given
 constexpr int kMaxPieces = kMaxSpans;// most pieces a stream row is cut into
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -113,7 +113,7 @@ struct __align__(16) SmemCore {
     uint32_t npend;                         // stream kernel: entries waiting in pend
     uint32_t flags;
     uint32_t kmax;
-    uint32_t ticket;
+    uint32_t ticket[2];                     // stream kernel: tickets of the split pieces
 };
 
 // The cluster leader's gather area: every span CTA pushes its list here.
@@ -593,20 +593,26 @@ __device__ __noinline__ void merge_pending(SmemCore &sm, const uint64_t *pend, i
     const uint64_t *run = sm.list[run_i];
     uint64_t *out = sm.list[out_i];
     const int total = np + run_len;
-    for (int t = tid; t < total; t += kThreads) {
-        const uint64_t x = t < np ? pend[t] : run[t - np];
+    // 2^sh threads (adjacent lanes) count for one entry, each over every 2^sh-th
+    // element; a butterfly adds their counts
+    const int sh = total <= kThreads / 4 ? 2 : (total <= kThreads / 2 ? 1 : 0);
+    const int sub = tid & ((1 << sh) - 1);
+    for (int t0 = 0; t0 < total; t0 += kThreads >> sh) {
+        const int t = t0 + (tid >> sh);
+        const bool valid = t < total;
+        uint64_t x = 0;
         uint32_t g = 0;
-        int u = 0;
-        for (; u + 1 < np; u += 2) {
-            const ulonglong2 p2 = *reinterpret_cast<const ulonglong2 *>(pend + u);
-            g += (p2.x > x) + (p2.y > x);
+        if (valid) {
+            x = t < np ? pend[t] : run[t - np];
+            for (int u = sub; u < np; u += 1 << sh) g += pend[u] > x;
+            if (t < np)
+                for (int u = sub; u < run_len; u += 1 << sh) g += run[u] > x;
         }
-        if (u < np) g += pend[u] > x;
-        if (t < np) {
-            const int pos = (int)g + count_greater(run, run_len, x);
+        if (sh >= 1) g += __shfl_xor_sync(0xFFFFFFFFu, g, 1);
+        if (sh >= 2) g += __shfl_xor_sync(0xFFFFFFFFu, g, 2);
+        if (valid && sub == 0) {
+            const int pos = (int)g + (t < np ? 0 : t - np);
             if (pos < k) out[pos] = x;
-        } else if ((t - np) + (int)g < k) {
-            out[(t - np) + g] = x;
         }
     }
     __syncthreads();
@@ -747,6 +753,57 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 // ---------------------------------------------------------------- stream kernel
 
+// The last CTA to finish a piece of row r: load the np published piece lists
+// (CTAs first..first+np-1, each list at most k entries, descending) into
+// `buf` in one pass, then place every entry at its rank in the union (its
+// position in its own list plus the entries of the other lists above it) and
+// write the row.  Block-uniform; `buf` holds np * (kMaxK + 1) entries.
+__device__ __noinline__ void fold_pieces(int64_t r, int64_t first, int np, int64_t per, int32_t nvr,
+                                         int k, const uint64_t *partials, uint64_t *buf,
+                                         int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                                         uint32_t *out_mask)
+{
+    const int tid = threadIdx.x;
+    constexpr int kW = kMaxK + 1;
+    for (int t = tid; t < np * (k + 1); t += kThreads) {
+        const int j = t / (k + 1), e = t - j * (k + 1);
+        const int64_t cta = first + j;
+        const int sl = (cta * per) / nvr == r ? 0 : 1;
+        buf[j * kW + e] = __ldcg(partials + (size_t)(cta * 2 + sl) * kW + e);
+    }
+    __syncthreads();
+    int total = 0;
+    uint32_t flags = 0;
+    for (int j = 0; j < np; ++j) {
+        const uint64_t h = buf[j * kW];
+        total += (int)(uint32_t)h;
+        flags |= (uint32_t)(h >> 32);
+    }
+    for (int t = tid; t < np * kMaxK; t += kThreads) {
+        const int j = t / kMaxK, p = t - j * kMaxK;
+        const uint64_t *lj = buf + j * kW + 1;
+        if (p >= (int)(uint32_t)buf[j * kW]) continue;
+        const uint64_t x = lj[p];
+        int pos = p;
+        for (int i = 0; i < np && pos < k; ++i)
+            if (i != j) pos += count_greater(buf + i * kW + 1, (int)(uint32_t)buf[i * kW], x);
+        if (pos < k) {
+            out_idx[r * k + pos] = entry_col(x);
+            out_val[r * k + pos] = (uint16_t)(x & 0xFFFFu);
+        }
+    }
+    const int cnt = min(k, total);
+    for (int t = cnt + tid; t < k; t += kThreads) {
+        out_idx[r * k + t] = -1;
+        out_val[r * k + t] = (uint16_t)kEmptyVal;
+    }
+    if (tid == 0) {
+        out_count[r] = cnt;
+        out_mask[r] = flags;
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
 topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
                    int32_t nvr, int64_t total, int64_t per, int32_t *__restrict__ out_idx,
@@ -809,6 +866,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
     int64_t row = row0; // the consumer's own cursor (thread 0's producer cursor runs ahead)
     int32_t vb = (int32_t)(g0 - row0 * nvr);
     int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
+    int64_t split0 = -1, split1 = -1; // rows this range holds only a piece of (first, last)
     while (g < g1 && !aborted) {
         const int32_t ve = (int32_t)min((int64_t)nvr, (int64_t)vb + (g1 - g));
         const ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
@@ -941,54 +999,19 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
 
         // ---- end of a row piece
         const int len = run_len;
-        const uint32_t flags = sm.flags;
         if (vb == 0 && ve == nvr) {
-            write_row(row, sm.list[run_i], len, flags, k, out_idx, out_val, out_count, out_mask);
+            write_row(row, sm.list[run_i], len, sm.flags, k, out_idx, out_val, out_count, out_mask);
         } else {
-            // publish this piece's list, then take a ticket for the row
-            const int slot = (g0 / nvr == row) ? 0 : 1;
+            // publish this piece's list (plain stores); its ticket is taken once
+            // the whole range is done, so the stream of chunks never stalls here
+            const int slot = row == row0 ? 0 : 1;
             uint64_t *mine = partials + (size_t)(b * 2 + slot) * (kMaxK + 1);
             for (int t = tid; t < len; t += kThreads) mine[1 + t] = sm.list[run_i][t];
-            if (tid == 0) mine[0] = (uint64_t)(uint32_t)len | ((uint64_t)flags << 32);
-            __syncthreads();
-            const int64_t first = (row * nvr) / per;
-            const int64_t last = min((int64_t)gridDim.x - 1, ((row + 1) * nvr - 1) / per);
-            const int np = (int)(last - first + 1);
-            if (tid == 0) {
-                __threadfence();
-                sm.ticket = atomicAdd(&tickets[first], 1u);
-            }
-            __syncthreads();
-            if (sm.ticket == (uint32_t)(np - 1)) {
-                // last piece in: fold every piece of this row into one list
-                __threadfence();
-                int rl = 0, ri = 0, ci = 1, fi = 2;
-                uint32_t fl = 0;
-                for (int j = 0; j < np; ++j) {
-                    const int64_t cta = first + j;
-                    const int sl = ((cta * per) / nvr == row) ? 0 : 1;
-                    const uint64_t *p = partials + (size_t)(cta * 2 + sl) * (kMaxK + 1);
-                    const uint64_t hdr = __ldcg(p);
-                    const int lj = (int)(uint32_t)hdr;
-                    fl |= (uint32_t)(hdr >> 32);
-                    uint64_t *dst = sm.list[rl == 0 ? ri : ci];
-                    for (int t = tid; t < lj; t += kThreads) dst[t] = __ldcg(p + 1 + t);
-                    __syncthreads();
-                    if (rl == 0) {
-                        rl = lj;
-                    } else if (lj > 0) {
-                        merge_lists(sm.list[ri], rl, sm.list[ci], lj, sm.list[fi], k);
-                        const int t = ri;
-                        ri = fi;
-                        fi = t;
-                        rl = min(k, rl + lj);
-                    }
-                    __syncthreads();
-                }
-                write_row(row, sm.list[ri], rl, fl, k, out_idx, out_val, out_count, out_mask);
-                if (tid == 0) tickets[first] = 0; // ready for the next call
-            }
-            __syncthreads();
+            if (tid == 0) mine[0] = (uint64_t)(uint32_t)len | ((uint64_t)sm.flags << 32);
+            if (slot == 0)
+                split0 = row;
+            else
+                split1 = row;
         }
         g += ve - vb;
         if (ve == nvr) {
@@ -996,6 +1019,34 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
             vb = 0;
         } else {
             vb = ve;
+        }
+    }
+
+    if (!aborted && (split0 >= 0 || split1 >= 0)) {
+        // every piece is published: one fence, then a ticket per split row; the
+        // last piece in for a row folds all of its pieces
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            uint32_t t0 = 0, t1 = 0;
+            if (split0 >= 0) t0 = atomicAdd(&tickets[(split0 * nvr) / per], 1u);
+            if (split1 >= 0) t1 = atomicAdd(&tickets[(split1 * nvr) / per], 1u);
+            sm.ticket[0] = t0;
+            sm.ticket[1] = t1;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int64_t r = s == 0 ? split0 : split1;
+            if (r < 0) continue;
+            const int64_t first = (r * nvr) / per;
+            const int64_t last = min((int64_t)gridDim.x - 1, ((r + 1) * nvr - 1) / per);
+            const int np = (int)(last - first + 1);
+            if (sm.ticket[s] != (uint32_t)(np - 1)) continue;
+            __threadfence();
+            fold_pieces(r, first, np, per, nvr, k, partials, reinterpret_cast<uint64_t *>(stages),
+                        out_idx, out_val, out_count, out_mask);
+            if (tid == 0) tickets[first] = 0; // ready for the next call
         }
     }
 
