@@ -138,6 +138,40 @@ int32_t tf_topk_bf16_max_spans(void);     /* == TF_TOPK_MAX_SPANS */
 int32_t tf_topk_bf16_cta_threads(void);   /* threads per CTA */
 int32_t tf_topk_bf16_chunk_columns(void); /* columns one CTA holds in registers per pass */
 
+/*
+ * Allocation-free variant of tf_topk_bf16.
+ *
+ * The paper has no counterpart: this entry point exists for callers that must
+ * not allocate device memory once they are running -- serving engines that
+ * reserve nearly all of HBM for their caches up front (a late cudaMalloc can
+ * fail there), and hosts of custom operators that hand a kernel only the
+ * buffers they own.  tf_topk_bf16 allocates its per-stream scratch on the
+ * first call on each stream (and frees and regrows it if a later call needs
+ * more); this call never allocates or frees anything.
+ *
+ * Same arguments, same results as tf_topk_bf16 (always the stream plan).  Its
+ * scratch is one static device array built into the library: room for
+ * TF_TOPK_NOALLOC_MAX_CTAS CTAs, two k-entry lists and a ticket each
+ * (534,528 bytes), held by every GPU that loads the library until the process
+ * exits.  A call needs one slot per CTA of its launch, at most twice the SM
+ * count of the device (304 on a 152-SM GB300); a call that would need more
+ * returns TF_TOPK_ERR_SCRATCH and launches nothing.
+ *
+ * The first call on each device looks up that device's address of the array
+ * (a host-side lookup, no allocation); make that first call before any stream
+ * capture begins.  Every call clears the tickets it uses (an asynchronous
+ * memset on `stream`) before its launch.  All calls share the one array:
+ * calls whose work overlaps on the GPU -- on different streams, or from
+ * different host threads without ordering -- race and give wrong results.
+ * Order them on one stream, or use tf_topk_bf16, whose scratch is per stream.
+ */
+#define TF_TOPK_NOALLOC_MAX_CTAS 512
+#define TF_TOPK_ERR_SCRATCH 8 /* tf_topk_bf16_noalloc: the launch would need more
+                                 than TF_TOPK_NOALLOC_MAX_CTAS scratch slots */
+int tf_topk_bf16_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                         int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                         uint32_t *out_nonfinite_mask, void *stream);
+
 /* Human-readable text for a TF_TOPK_* status (static storage). */
 const char *tf_topk_strerror(int status);
 

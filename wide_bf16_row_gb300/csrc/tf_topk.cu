@@ -56,9 +56,20 @@
 #include <map>
 #include <mutex>
 #include <thread>
+
 #include <utility>
 
 #include "tf_topk.h"
+
+// Scratch of tf_topk_bf16_noalloc, for callers that may not allocate: per CTA
+// slot two partial lists of (TF_TOPK_MAX_K + 1) 64-bit words, then one 32-bit
+// ticket per slot.  Host code reaches it only through the address
+// cudaGetSymbolAddress returns for the current device.
+constexpr size_t kNoAllocListWords = (size_t)TF_TOPK_NOALLOC_MAX_CTAS * 2 * (TF_TOPK_MAX_K + 1);
+constexpr size_t kNoAllocWords = kNoAllocListWords + TF_TOPK_NOALLOC_MAX_CTAS / 2;
+static_assert(TF_TOPK_NOALLOC_MAX_CTAS % 2 == 0, "tickets fill whole 64-bit words");
+static_assert(kNoAllocListWords * 8 % 256 == 0, "the ticket block starts 256-byte aligned");
+static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocWords];
 
 namespace cg = cooperative_groups;
 
@@ -1418,6 +1429,55 @@ int run(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int3
     return TF_TOPK_OK;
 }
 
+// tf_topk_bf16_noalloc: the device address of g_noalloc_scratch, looked up
+// once per device (with that device current) and kept.
+std::mutex g_noalloc_mutex;
+uint64_t *g_noalloc_addr[kMaxDevices];
+
+int noalloc_scratch(int dev, uint64_t **out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e);
+        g_noalloc_addr[dev] = static_cast<uint64_t *>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return TF_TOPK_OK;
+}
+
+// The stream plan with its scratch in the static array: no allocation, no free.
+int run_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_mask, void *stream)
+{
+    int st = validate(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask);
+    if (st != TF_TOPK_OK) return st;
+    if (rows == 0) return TF_TOPK_OK;
+    int dev = 0, sm_count = 0;
+    st = device_setup(&dev, &sm_count);
+    if (st != TF_TOPK_OK) return st;
+    int64_t per = 0, ctas = 0;
+    stream_geometry(rows, cols, sm_count, false, &per, &ctas);
+    if (ctas > TF_TOPK_NOALLOC_MAX_CTAS) return TF_TOPK_ERR_SCRATCH;
+    uint64_t *base = nullptr;
+    st = noalloc_scratch(dev, &base);
+    if (st != TF_TOPK_OK) return st;
+    uint64_t *partials = base;
+    uint32_t *tickets = reinterpret_cast<uint32_t *>(base + kNoAllocListWords);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the previous call may have been cut short with tickets half counted
+    cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)ctas * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    const int32_t nvr = vectors_per_row(cols);
+    topk_stream_kernel<<<(unsigned)ctas, kThreads, kStreamSmemBytes, s>>>(
+        static_cast<const uint16_t *>(logits), (int32_t)cols, row_stride, k, nvr, rows * nvr, per, out_idx,
+        out_val, out_count, out_mask, partials, tickets);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e);
+    return TF_TOPK_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -1436,6 +1496,14 @@ int tf_topk_bf16_with_plan(const void *logits, int64_t rows, int64_t cols, int64
 {
     return run(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask, plan,
                stream);
+}
+
+int tf_topk_bf16_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                         int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask,
+                         void *stream)
+{
+    return run_noalloc(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask,
+                       stream);
 }
 
 int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)
@@ -1486,6 +1554,8 @@ const char *tf_topk_strerror(int status)
     case TF_TOPK_ERR_PLAN: return "unknown plan code";
     case TF_TOPK_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
     case TF_TOPK_ERR_CUDA: return "CUDA runtime error (see tf_topk_last_cuda_error)";
+    case TF_TOPK_ERR_SCRATCH: return "the launch needs more scratch slots than the static area of "
+                                     "tf_topk_bf16_noalloc holds (TF_TOPK_NOALLOC_MAX_CTAS)";
     default: return "unknown status";
     }
 }

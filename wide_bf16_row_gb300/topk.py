@@ -14,6 +14,7 @@ LIBRARY = PKG / "libtf_topk.so"
 
 # status codes (include/tf_topk.h)
 OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_PLAN, ERR_DEVICE, ERR_CUDA = range(8)
+ERR_SCRATCH = 8  # tf_topk_bf16_noalloc only
 
 # launch plans (include/tf_topk.h)
 PLAN_AUTO, PLAN_SINGLE, PLAN_STREAM = 0, 1, 32
@@ -43,6 +44,8 @@ def library() -> ctypes.CDLL:
         lib.tf_topk_bf16_with_plan.restype = ctypes.c_int
         lib.tf_topk_bf16_with_plan.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p,
                                                c_p, c_i32, c_p]
+        lib.tf_topk_bf16_noalloc.restype = ctypes.c_int
+        lib.tf_topk_bf16_noalloc.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
         lib.tf_topk_device_fault.restype = ctypes.c_int
         lib.tf_topk_device_fault.argtypes = []
         lib.tf_topk_bf16_plan.restype = c_i32
@@ -97,6 +100,15 @@ def tf_topk_bf16_with_plan(logits: int, rows: int, cols: int, row_stride: int, k
     """The C entry point with an explicit launch plan; returns the status code."""
     return library().tf_topk_bf16_with_plan(logits, rows, cols, row_stride, k, out_idx, out_val,
                                             out_count, out_nonfinite_mask, plan, stream)
+
+
+def tf_topk_bf16_noalloc(logits: int, rows: int, cols: int, row_stride: int, k: int,
+                         out_idx: int, out_val: int, out_count: int, out_nonfinite_mask: int,
+                         stream: int | None) -> int:
+    """The allocation-free C entry point (static scratch shared by every call;
+    calls that overlap on the GPU race); returns the status code."""
+    return library().tf_topk_bf16_noalloc(logits, rows, cols, row_stride, k, out_idx, out_val,
+                                          out_count, out_nonfinite_mask, stream)
 
 
 def device_fault() -> int:
