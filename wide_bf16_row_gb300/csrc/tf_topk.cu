@@ -100,6 +100,7 @@ static_assert((kMaxK + kWarps - 1) / kWarps <= 32, "per-warp order statistic nee
 static_assert(kMaxSpans == 16 && (kMaxSpans & (kMaxSpans - 1)) == 0, "merge tree over 2^n lists");
 static_assert(kMaxK == 64, "header and kernels agree on max_k");
 static_assert(kStages >= 2, "a ring needs two stages");
+static_assert(kMinVecsPerCta >= 4 * kThreads, "moved range starts stay strictly increasing");
 static_assert(kVecPerThread * 4 == 32, "the candidate scan maps a lane to one word of a thread's slice");
 
 constexpr uint32_t kEmptyVal = 0x7FC0;
@@ -474,6 +475,42 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
 // Selection for one chunk whose keys are in kv (see chunk_keys) with this
 // thread's max key tmax: the row piece's running list (run_i, run_len)
 // absorbs the chunk's top-k.  Block-uniform: every thread calls it.
+// Prefilter bound of one chunk (block-uniform, one barrier).  The fw warps
+// whose 32 lanes all hold data each find the j-th largest of their lanes'
+// maxima, j = ceil(k / fw); the minimum t0 over them is reached by at least
+// fw * j >= k elements of the chunk, so no element below t0 can be in the
+// top k of anything that contains the chunk.  With no such bound (a tiny
+// chunk, or a warp without j positive maxima) the result is 0.
+__device__ __forceinline__ uint32_t prefilter_bound(uint32_t tmax, int nvalid, int k, SmemCore &sm)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int fw = min(nvalid, kThreads) / 32;
+    const int j = fw ? (k + fw - 1) / fw : 33;
+    uint32_t tw = 0xFFFFu; // warps without a full set of lanes do not bound
+    if (warp < fw) {
+        tw = 0;
+        if (j <= 32) {
+            uint32_t v = tmax, cnt = 0;
+            for (int it = 0; it < j; ++it) {
+                const uint32_t mval = __reduce_max_sync(0xFFFFFFFFu, v);
+                if (mval == 0) break;
+                cnt += __popc(__ballot_sync(0xFFFFFFFFu, v == mval));
+                if (cnt >= (uint32_t)j) {
+                    tw = mval;
+                    break;
+                }
+                if (v == mval) v = 0;
+            }
+        }
+    }
+    if (lane == 0) sm.warp_t[warp] = tw;
+    __syncthreads();
+    uint32_t t0 = (fw == 0 || j > 32) ? 0u : 0xFFFFu;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
+    return t0;
+}
+
 __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, int nvalid,
                                              int32_t col_base, int k, SmemCore &sm, uint4 *stage,
                                              int &run_i, int &chunk_i, int &free_i, int &run_len)
@@ -486,37 +523,7 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
         // column of this chunk is higher), and that bound needs no barrier
         t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
     } else {
-        // ---- prefilter threshold.  The fw warps whose 32 lanes all hold data
-        //      each find the j-th largest of their lanes' maxima, j = ceil(k / fw);
-        //      the minimum t0 over them is reached by at least fw * j >= k
-        //      elements.  With no such bound (a tiny chunk, or a warp without j
-        //      positive maxima) t0 = 0 and every element is a candidate.
-        const int fw = min(nvalid, kThreads) / 32;
-        const int j = fw ? (k + fw - 1) / fw : 33;
-        uint32_t tw = 0xFFFFu; // warps without a full set of lanes do not bound
-        if (warp < fw) {
-            tw = 0;
-            if (j <= 32) {
-                uint32_t v = tmax, cnt = 0;
-                for (int it = 0; it < j; ++it) {
-                    const uint32_t mval = __reduce_max_sync(0xFFFFFFFFu, v);
-                    if (mval == 0) break;
-                    cnt += __popc(__ballot_sync(0xFFFFFFFFu, v == mval));
-                    if (cnt >= (uint32_t)j) {
-                        tw = mval;
-                        break;
-                    }
-                    if (v == mval) v = 0;
-                }
-            }
-        }
-        if (lane == 0) sm.warp_t[warp] = tw;
-        __syncthreads();
-        uint32_t t0 = (fw == 0 || j > 32) ? 0u : 0xFFFFu;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) t0 = min(t0, sm.warp_t[w]);
-        t_floor = max(key_floor(t0), 1u);
-        if (run_len > 0 && run_len == k) t_floor = max(t_floor, (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u);
+        t_floor = max(key_floor(prefilter_bound(tmax, nvalid, k, sm)), 1u);
     }
 
     // ---- candidates: only threads whose max reaches t_floor hold any; each
@@ -615,9 +622,24 @@ __device__ __noinline__ void merge_pending(SmemCore &sm, const uint64_t *pend, i
         uint32_t g = 0;
         if (valid) {
             x = t < np ? pend[t] : run[t - np];
-            for (int u = sub; u < np; u += 1 << sh) g += pend[u] > x;
-            if (t < np)
-                for (int u = sub; u < run_len; u += 1 << sh) g += run[u] > x;
+            const int step = 1 << sh;
+            uint32_t g1 = 0, g2 = 0, g3 = 0;
+            int u = sub;
+            for (; u + 3 * step < np; u += 4 * step) {
+                g += pend[u] > x;
+                g1 += pend[u + step] > x;
+                g2 += pend[u + 2 * step] > x;
+                g3 += pend[u + 3 * step] > x;
+            }
+            for (; u < np; u += step) g += pend[u] > x;
+            if (t < np) {
+                for (u = sub; u + step < run_len; u += 2 * step) {
+                    g1 += run[u] > x;
+                    g2 += run[u + step] > x;
+                }
+                if (u < run_len) g3 += run[u] > x;
+            }
+            g += g1 + g2 + g3;
         }
         if (sh >= 1) g += __shfl_xor_sync(0xFFFFFFFFu, g, 1);
         if (sh >= 2) g += __shfl_xor_sync(0xFFFFFFFFu, g, 2);
@@ -635,20 +657,40 @@ __device__ __noinline__ void merge_pending(SmemCore &sm, const uint64_t *pend, i
     __syncthreads();
 }
 
-// Stream kernel, steady state: a chunk whose candidates overflowed the pending
-// buffer.  Its keys are still in its stage (written back there, 0 where
-// nothing may be selected); select its best k exactly over the keys that reach
-// t_floor and put them into pend[np_before..np_before + k).  Returns the new
-// pending count.  Block-uniform.
+// Stream kernel: a chunk whose candidates overflowed the pending buffer.  Its
+// stage is not refilled yet, but only partly holds keys, so the chunk is read
+// again from global memory (rare: heavy ties) and its keys staged in column
+// order, 0 where nothing may be selected; then its best k over the keys that
+// reach t_floor are selected exactly and put into pend[np_before ..
+// np_before + k).  Returns the new pending count.  Block-uniform.
 __device__ __noinline__ int lazy_overflow(SmemCore &sm, uint64_t *pend, uint4 *stage, uint32_t t_floor,
-                                          int32_t col_base, int np_before, int k)
+                                          ChunkGeom geo, int32_t cb, int nvalid, int np_before, int k)
 {
     const int tid = threadIdx.x;
+    const int32_t col_base = cb * 8 - geo.m;
+    const uint4 *rowv = reinterpret_cast<const uint4 *>(geo.rowp - geo.m);
+    uint32_t kv[kVecPerThread][4];
+#pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
-        uint4 q = stage[i * kThreads + tid];
-        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        const int lv = i * kThreads + tid;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (lv < nvalid) {
+            const int32_t v = cb + lv;
+            q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(rowv + v)
+                                                   : load_edge_vector(geo.rowp, geo.cols, geo.m, v);
+        }
+        kv[i][0] = q.x;
+        kv[i][1] = q.y;
+        kv[i][2] = q.z;
+        kv[i][3] = q.w;
+    }
+    chunk_keys<false>(kv, nvalid, col_base, geo.cols, stage, sm);
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+        uint32_t w[4];
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t lo = w[j] & 0xFFFFu, hi = w[j] >> 16;
+            const uint32_t lo = kv[i][j] & 0xFFFFu, hi = kv[i][j] >> 16;
             w[j] = (lo >= t_floor ? lo : 0u) | ((hi >= t_floor ? hi : 0u) << 16);
         }
         stage[i * kThreads + tid] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -764,13 +806,52 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 // ---------------------------------------------------------------- stream kernel
 
+// Stream-plan ranges.  CTA b nominally starts at vector b * per of the
+// rows x vectors space; the start is moved to the nearest multiple of kThreads
+// vectors from its row's start, or to the row's end when less than kThreads
+// vectors would be left there.  So every piece of a row holds at least
+// kThreads vectors (unless the whole row is shorter) and its first chunk
+// always yields a prefilter bound.  Starts move by at most kThreads/2 back or
+// 3*kThreads/2 forward, and per >= 4*kThreads, so they strictly increase up
+// to `total`.
+__device__ __forceinline__ int64_t range_start(int64_t b, int64_t per, int64_t total, int32_t nvr)
+{
+    const int64_t x = b * per;
+    if (x >= total) return total;
+    const int64_t r = x / nvr;
+    const int32_t off = (int32_t)(x - r * nvr);
+    int32_t cut = (off + kThreads / 2) / kThreads * kThreads;
+    if (cut != 0 && nvr - cut < kThreads) cut = nvr;
+    return min(total, r * nvr + cut);
+}
+
+// Take a ticket: an atomic increment with release semantics for the piece
+// lists this CTA published before it (other threads' stores are ordered
+// before it by the preceding barrier) and acquire semantics for the lists of
+// the CTAs that took earlier tickets (the caller's barrier then hands them
+// to the whole CTA).  Returns the old count.
+__device__ __forceinline__ uint32_t ticket_add(uint32_t *t)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+    return old;
+}
+
+// The CTA whose range holds vector y (the last CTA whose start is <= y).
+__device__ __forceinline__ int64_t range_of(int64_t y, int64_t per, int64_t total, int32_t nvr, int64_t ctas)
+{
+    int64_t b = min(ctas - 1, y / per + 1);
+    while (b > 0 && range_start(b, per, total, nvr) > y) --b;
+    return b;
+}
+
 // The last CTA to finish a piece of row r: load the np published piece lists
 // (CTAs first..first+np-1, each list at most k entries, descending) into
 // `buf` in one pass, then place every entry at its rank in the union (its
 // position in its own list plus the entries of the other lists above it) and
 // write the row.  Block-uniform; `buf` holds np * (kMaxK + 1) entries.
-__device__ __noinline__ void fold_pieces(int64_t r, int64_t first, int np, int64_t per, int32_t nvr,
-                                         int k, const uint64_t *partials, uint64_t *buf,
+__device__ __noinline__ void fold_pieces(int64_t r, int64_t first, int np, int64_t per, int64_t total,
+                                         int32_t nvr, int k, const uint64_t *partials, uint64_t *buf,
                                          int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
                                          uint32_t *out_mask)
 {
@@ -779,15 +860,15 @@ __device__ __noinline__ void fold_pieces(int64_t r, int64_t first, int np, int64
     for (int t = tid; t < np * (k + 1); t += kThreads) {
         const int j = t / (k + 1), e = t - j * (k + 1);
         const int64_t cta = first + j;
-        const int sl = (cta * per) / nvr == r ? 0 : 1;
+        const int sl = range_start(cta, per, total, nvr) / nvr == r ? 0 : 1;
         buf[j * kW + e] = __ldcg(partials + (size_t)(cta * 2 + sl) * kW + e);
     }
     __syncthreads();
-    int total = 0;
+    int entries = 0;
     uint32_t flags = 0;
     for (int j = 0; j < np; ++j) {
         const uint64_t h = buf[j * kW];
-        total += (int)(uint32_t)h;
+        entries += (int)(uint32_t)h;
         flags |= (uint32_t)(h >> 32);
     }
     for (int t = tid; t < np * kMaxK; t += kThreads) {
@@ -803,7 +884,7 @@ __device__ __noinline__ void fold_pieces(int64_t r, int64_t first, int np, int64
             out_val[r * k + pos] = (uint16_t)(x & 0xFFFFu);
         }
     }
-    const int cnt = min(k, total);
+    const int cnt = min(k, entries);
     for (int t = cnt + tid; t < k; t += kThreads) {
         out_idx[r * k + t] = -1;
         out_val[r * k + t] = (uint16_t)kEmptyVal;
@@ -827,8 +908,9 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
     SmemCore &sm = *reinterpret_cast<SmemCore *>(dsmem + (size_t)kStages * kChunkVecs * 16);
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.x;
-    const int64_t g0 = b * per;
-    const int64_t g1 = min(total, g0 + per);
+    const int64_t ctas = gridDim.x;
+    const int64_t g0 = range_start(b, per, total, nvr);
+    const int64_t g1 = range_start(b + 1, per, total, nvr);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&sm.mbar[s], 1);
@@ -876,7 +958,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
     int64_t g = g0;
     int64_t row = row0; // the consumer's own cursor (thread 0's producer cursor runs ahead)
     int32_t vb = (int32_t)(g0 - row0 * nvr);
-    int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
+    int run_i = 0, free_i = 1, run_len = 0;
     int64_t split0 = -1, split1 = -1; // rows this range holds only a piece of (first, last)
     while (g < g1 && !aborted) {
         const int32_t ve = (int32_t)min((int64_t)nvr, (int64_t)vb + (g1 - g));
@@ -886,25 +968,28 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
             sm.npend = 0;
         }
         run_i = 0;
-        chunk_i = 1;
-        free_i = 2;
+        free_i = 1;
         run_len = 0;
-        // the previous chunk, when it only pushed its candidates (steady state)
+        // the previous chunk, whose candidates wait in the pending buffer
         bool prev_lazy = false;
         uint4 *prev_st = nullptr;
         uint32_t prev_t = 0;
-        int32_t prev_col_base = 0;
+        int32_t prev_cb = 0;
+        int prev_nvalid = 0;
         int prev_np0 = 0;
+        // a bound valid for the rest of the piece: at least k of its columns
+        // seen so far score at least this (0: none yet)
+        uint32_t t_piece = 0;
 
-        // Pending candidates of the previous lazy chunk: an overflow is
-        // re-selected exactly from its stage (not yet refilled) and merged; a
-        // full enough buffer is merged.  `at_end`: merge whatever waits.
-        // Returns the pending count afterwards (the same in every thread).
+        // Pending candidates of the previous chunk: an overflow is re-selected
+        // exactly and merged; a full enough buffer is merged.  `at_end`: merge
+        // whatever waits.  Returns the pending count afterwards (the same in
+        // every thread).
         auto settle = [&](bool at_end) -> int {
             int np = (int)sm.npend;
             bool force = at_end;
             if (np > kPendCap) {
-                np = lazy_overflow(sm, pend, prev_st, prev_t, prev_col_base, prev_np0, k);
+                np = lazy_overflow(sm, pend, prev_st, prev_t, geo, prev_cb, prev_nvalid, prev_np0, k);
                 force = true;
             }
             if (np >= kMergeAt || (force && np > 0)) {
@@ -964,43 +1049,72 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                 }
                 tmax = chunk_keys<false>(kv, nvalid, col_base, cols, st, sm);
             }
-            if (run_len < k) {
-                // the piece's first chunks: a prefilter bound and an immediate merge
-                select_chunk(kv, tmax, nvalid, col_base, k, sm, st, run_i, chunk_i, free_i, run_len);
-                prev_lazy = false;
+            // A new entry must beat the running k-th strictly once the piece has
+            // k entries (every column of this chunk is higher); before that, a
+            // prefilter bound of the first chunk that has one.  Candidates go to
+            // the pending buffer as list entries, with no barrier: only threads
+            // whose max reaches the bound spill their keys, and their warp scans
+            // them one word per lane.
+            uint32_t t_floor;
+            if (run_len == k) {
+                t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
+            } else if (t_piece != 0) {
+                t_floor = t_piece;
             } else {
-                // steady state: a new entry must beat the running k-th strictly
-                // (every column of this chunk is higher).  Candidates are rare; they
-                // go to the pending buffer as list entries, with no barrier.  The
-                // keys are written back over the stage in case the buffer overflows.
-                const uint32_t t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
+                const uint32_t t0 = prefilter_bound(tmax, nvalid, k, sm);
+                t_floor = max(key_floor(t0), 1u);
+                if (t0 != 0) t_piece = t_floor;
+            }
+            const bool hit = tmax >= t_floor;
+            if (hit) {
 #pragma unroll
                 for (int i = 0; i < kVecPerThread; ++i)
                     st[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
-                __syncwarp();
+            }
+            __syncwarp();
+            {
+                // two spilled threads per step; one atomic reserves the step's slots
                 const int lane = tid & 31, warp = tid >> 5;
-                for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, tmax >= t_floor); hits; hits &= hits - 1) {
-                    const int src = warp * 32 + __ffs(hits) - 1;
-                    const int lv = (lane >> 2) * kThreads + src;
-                    const uint32_t key2 = reinterpret_cast<const uint32_t *>(st)[lv * 4 + (lane & 3)];
-                    const int32_t col0 = col_base + lv * 8 + 2 * (lane & 3);
-                    const uint32_t klo = key2 & 0xFFFFu, khi = key2 >> 16;
-                    if (klo >= t_floor) {
-                        const uint32_t slot = atomicAdd(&sm.npend, 1u);
-                        if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(klo, col0);
+                const uint32_t lt = (1u << lane) - 1u;
+                const uint32_t *words = reinterpret_cast<const uint32_t *>(st);
+                for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits;) {
+                    const int sa = __ffs(hits) - 1;
+                    hits &= hits - 1;
+                    const int sb = hits ? __ffs(hits) - 1 : -1;
+                    if (hits) hits &= hits - 1;
+                    const int lva = (lane >> 2) * kThreads + warp * 32 + sa;
+                    const int lvb = (lane >> 2) * kThreads + warp * 32 + (sb < 0 ? sa : sb);
+                    const uint32_t ka = words[lva * 4 + (lane & 3)];
+                    const uint32_t kb = sb < 0 ? 0u : words[lvb * 4 + (lane & 3)];
+                    const uint32_t e[4] = {ka & 0xFFFFu, ka >> 16, kb & 0xFFFFu, kb >> 16};
+                    uint32_t m[4], n = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        m[q] = __ballot_sync(0xFFFFFFFFu, e[q] >= t_floor);
+                        n += __popc(m[q]);
                     }
-                    if (khi >= t_floor) {
-                        const uint32_t slot = atomicAdd(&sm.npend, 1u);
-                        if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(khi, col0 + 1);
+                    uint32_t base = 0;
+                    if (lane == 0 && n) base = atomicAdd(&sm.npend, n);
+                    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (e[q] >= t_floor) {
+                            const uint32_t slot = base + __popc(m[q] & lt);
+                            const int32_t col = col_base + (q < 2 ? lva : lvb) * 8 + 2 * (lane & 3) + (q & 1);
+                            if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(e[q], col);
+                        }
+                        base += __popc(m[q]);
                     }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                prev_lazy = true;
-                prev_st = st;
-                prev_t = t_floor;
-                prev_col_base = col_base;
-                prev_np0 = np_now;
             }
+            // the stage is next written by a bulk copy (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            prev_lazy = true;
+            prev_st = st;
+            prev_t = t_floor;
+            prev_cb = cb;
+            prev_nvalid = nvalid;
+            prev_np0 = np_now;
             ++c;
         }
         if (aborted) break;
@@ -1038,10 +1152,9 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
         // last piece in for a row folds all of its pieces
         __syncthreads();
         if (tid == 0) {
-            __threadfence();
             uint32_t t0 = 0, t1 = 0;
-            if (split0 >= 0) t0 = atomicAdd(&tickets[(split0 * nvr) / per], 1u);
-            if (split1 >= 0) t1 = atomicAdd(&tickets[(split1 * nvr) / per], 1u);
+            if (split0 >= 0) t0 = ticket_add(&tickets[range_of(split0 * nvr, per, total, nvr, ctas)]);
+            if (split1 >= 0) t1 = ticket_add(&tickets[range_of(split1 * nvr, per, total, nvr, ctas)]);
             sm.ticket[0] = t0;
             sm.ticket[1] = t1;
         }
@@ -1050,12 +1163,11 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
         for (int s = 0; s < 2; ++s) {
             const int64_t r = s == 0 ? split0 : split1;
             if (r < 0) continue;
-            const int64_t first = (r * nvr) / per;
-            const int64_t last = min((int64_t)gridDim.x - 1, ((r + 1) * nvr - 1) / per);
+            const int64_t first = range_of(r * nvr, per, total, nvr, ctas);
+            const int64_t last = range_of((r + 1) * nvr - 1, per, total, nvr, ctas);
             const int np = (int)(last - first + 1);
             if (sm.ticket[s] != (uint32_t)(np - 1)) continue;
-            __threadfence();
-            fold_pieces(r, first, np, per, nvr, k, partials, reinterpret_cast<uint64_t *>(stages),
+            fold_pieces(r, first, np, per, total, nvr, k, partials, reinterpret_cast<uint64_t *>(stages),
                         out_idx, out_val, out_count, out_mask);
             if (tid == 0) tickets[first] = 0; // ready for the next call
         }
@@ -1314,7 +1426,8 @@ void stream_geometry(int64_t rows, int64_t cols, int sm_count, bool one_row_per_
         const int64_t slots = (int64_t)sm_count * kStreamCtasPerSm;
         per = (total + slots - 1) / slots;
         per = per < kMinVecsPerCta ? kMinVecsPerCta : per;
-        const int64_t min_piece = (nvr + kMaxPieces - 2) / (kMaxPieces - 1); // a row meets <= kMaxPieces CTAs
+        // a row meets <= kMaxPieces CTAs, after range starts move by up to 2 * kThreads
+        const int64_t min_piece = (nvr + kMaxPieces - 2) / (kMaxPieces - 1) + 2 * kThreads;
         per = per < min_piece ? min_piece : per;
     }
     *per_out = per;
