@@ -83,18 +83,22 @@ extern "C" {
  * All buffers are owned by the caller; outputs must not overlap the input.
  * The call runs on the current CUDA device.  Returns a TF_TOPK_* status.
  *
- * Scratch: the default (stream) plan keeps a small per-(device, stream) area
- * (two k-entry lists and a ticket per CTA, under 1 MB) that the library
- * allocates on the first call on that stream and keeps until exit.  That first
- * call therefore allocates (cudaMalloc) and should not be made during stream
- * capture.  Outputs are never allocated by the library.
+ * Scratch: the plans this call picks need none.  The stream plan
+ * (TF_TOPK_PLAN_STREAM, only through tf_topk_bf16_with_plan) keeps a small
+ * per-(device, stream) area (two k-entry lists and a ticket per CTA, under
+ * 1 MB) that the library allocates on its first call on that stream and keeps
+ * until exit; that first call therefore allocates (cudaMalloc) and should not
+ * be made during stream capture.  Outputs are never allocated by the library.
  */
 int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
                  int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
                  uint32_t *out_nonfinite_mask, void *stream);
 
 /* Launch plans (tf_topk_bf16_with_plan).  Every plan gives identical results. */
-#define TF_TOPK_PLAN_AUTO 0      /* what tf_topk_bf16 picks for the shape */
+#define TF_TOPK_PLAN_AUTO 0      /* what tf_topk_bf16 picks for the shape: CLUSTER2 with
+                                    at least one row per SM, else the cluster plan whose
+                                    grid reaches about two CTAs per SM without spans
+                                    narrower than half a chunk (measured on GB300) */
 #define TF_TOPK_PLAN_SINGLE 1    /* control: one CTA streams each whole row (the
                                     pages' single-group kernel) */
 #define TF_TOPK_PLAN_CLUSTER2 2  /* each row split into 2/4/8/16 column spans, one */
@@ -139,15 +143,15 @@ int32_t tf_topk_bf16_cta_threads(void);   /* threads per CTA */
 int32_t tf_topk_bf16_chunk_columns(void); /* columns one CTA holds in registers per pass */
 
 /*
- * Allocation-free variant of tf_topk_bf16.
+ * Allocation-free variant of the stream plan.
  *
  * The paper has no counterpart: this entry point exists for callers that must
  * not allocate device memory once they are running -- serving engines that
  * reserve nearly all of HBM for their caches up front (a late cudaMalloc can
  * fail there), and hosts of custom operators that hand a kernel only the
- * buffers they own.  tf_topk_bf16 allocates its per-stream scratch on the
- * first call on each stream (and frees and regrows it if a later call needs
- * more); this call never allocates or frees anything.
+ * buffers they own.  The stream plan of tf_topk_bf16_with_plan allocates its
+ * per-stream scratch on the first call on each stream (and frees and regrows
+ * it if a later call needs more); this call never allocates or frees anything.
  *
  * Same arguments, same results as tf_topk_bf16 (always the stream plan).  Its
  * scratch is one static device array built into the library: room for
@@ -163,7 +167,8 @@ int32_t tf_topk_bf16_chunk_columns(void); /* columns one CTA holds in registers 
  * memset on `stream`) before its launch.  All calls share the one array:
  * calls whose work overlaps on the GPU -- on different streams, or from
  * different host threads without ordering -- race and give wrong results.
- * Order them on one stream, or use tf_topk_bf16, whose scratch is per stream.
+ * Order them on one stream, or use tf_topk_bf16_with_plan, whose stream-plan
+ * scratch is per stream.
  */
 #define TF_TOPK_NOALLOC_MAX_CTAS 512
 #define TF_TOPK_ERR_SCRATCH 8 /* tf_topk_bf16_noalloc: the launch would need more

@@ -1434,12 +1434,20 @@ void stream_geometry(int64_t rows, int64_t cols, int sm_count, bool one_row_per_
     *ctas_out = (total + per - 1) / per;
 }
 
-int32_t pick_plan(int64_t rows, int64_t cols, int sm_count)
+// The plan tf_topk_bf16 uses.  Measured on GB300 over widths 4096..248320,
+// rows 1..1024 and every plan: the cluster plans are the fastest, or within
+// noise of it, everywhere.  With at least one row per SM two spans per row win;
+// with fewer rows, the span count that brings the grid to about two CTAs per
+// SM, but no span narrower than half a chunk (a whole chunk for k > 32, whose
+// merges cost more).
+int32_t pick_plan(int64_t rows, int64_t cols, int32_t k, int sm_count)
 {
-    (void)rows;
-    (void)cols;
-    (void)sm_count;
-    return TF_TOPK_PLAN_STREAM;
+    if (rows >= sm_count) return TF_TOPK_PLAN_CLUSTER2;
+    const int64_t min_span = k > 32 ? kChunkCols : kChunkCols / 2;
+    int s = 2;
+    while (s < kMaxSpans && rows * s < 2 * (int64_t)sm_count) s *= 2;
+    while (s > 2 && cols / s < min_span) s /= 2;
+    return s;
 }
 
 template <int S>
@@ -1512,7 +1520,7 @@ int run(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int3
     int dev = 0, sm_count = 0;
     st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return st;
-    if (plan == TF_TOPK_PLAN_AUTO) plan = pick_plan(rows, cols, sm_count);
+    if (plan == TF_TOPK_PLAN_AUTO) plan = pick_plan(rows, cols, k, sm_count);
     const uint16_t *x = static_cast<const uint16_t *>(logits);
     const int32_t c = (int32_t)cols;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1626,7 +1634,7 @@ int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)
     int dev = 0, sm_count = 0;
     const int st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return -st;
-    return pick_plan(rows, cols, sm_count);
+    return pick_plan(rows, cols, k, sm_count);
 }
 
 int tf_topk_device_fault(void)
