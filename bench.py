@@ -39,7 +39,10 @@ if str(ROOT) not in sys.path:
 METRIC = "rows/s and µs/call for bf16 row top-k; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "256x248320_k20"
 KERNEL_SOURCE = ROOT / "wide_bf16_row_gb300" / "csrc" / "tf_topk.cu"
-PROFILE_SUMMARY = ROOT / "profiles" / "topk_rows_kernel_256x248320_k20.md"
+PROFILES = ROOT / "profiles"
+# the kernel each launch plan runs (the ncu summaries are named after it)
+PLAN_KERNEL = {1: "topk_stream_kernel_rowwise", 2: "topk_cluster_kernel_S2", 4: "topk_cluster_kernel_S4",
+               8: "topk_cluster_kernel_S8", 16: "topk_cluster_kernel_S16", 32: "topk_stream_kernel"}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -82,12 +85,13 @@ def kernel_source_hash() -> str:
     return hashlib.sha256(KERNEL_SOURCE.read_bytes()).hexdigest()
 
 
-def profiled_traffic() -> int | None:
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def profiled_traffic(plan: int, workload: str) -> int | None:
+    """DRAM bytes per launch of the plan's kernel on this workload, from the
+    committed ncu summary, if it was taken on the current kernel source (else
+    None)."""
     try:
-        text = PROFILE_SUMMARY.read_text()
-    except OSError:
+        text = (PROFILES / f"{PLAN_KERNEL[plan]}_{workload}.md").read_text()
+    except (OSError, KeyError):
         return None
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
@@ -392,7 +396,7 @@ def run_ours(args) -> None:
             "us_per_call": avg_launch_s * 1e6,
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "frac": achieved / peak, "traffic": profiled_traffic(plan, w.name),
                          "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "launches_timed": len(launch_ms)},
