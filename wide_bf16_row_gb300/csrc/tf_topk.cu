@@ -604,6 +604,57 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
 // any order) into list[out_i]; the indices swap and the pending count is
 // cleared.  A rank merge: an entry's place is the number of larger pending
 // entries plus the number of larger running entries.  Block-uniform.
+// Push this chunk's keys that reach t_floor into the pending buffer as list
+// entries.  Threads whose max reaches t_floor spill their keys into their own
+// slots of `stage` (vector i at stage[i * kThreads + tid]); their warp scans
+// them one word per lane, two spilled threads per step, and one atomic per
+// step reserves the step's slots.  Entries past kPendCap are dropped (the
+// count still grows, so the caller sees the overflow).  No block barrier.
+__device__ __forceinline__ void push_pending(const uint32_t (&kv)[kVecPerThread][4], uint32_t tmax,
+                                             uint32_t t_floor, int32_t col_base, uint4 *stage,
+                                             SmemCore &sm, uint64_t *pend)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool hit = tmax >= t_floor;
+    if (hit) {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i)
+            stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+    }
+    __syncwarp();
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t *words = reinterpret_cast<const uint32_t *>(stage);
+    for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits;) {
+        const int sa = __ffs(hits) - 1;
+        hits &= hits - 1;
+        const int sb = hits ? __ffs(hits) - 1 : -1;
+        if (hits) hits &= hits - 1;
+        const int lva = (lane >> 2) * kThreads + warp * 32 + sa;
+        const int lvb = (lane >> 2) * kThreads + warp * 32 + (sb < 0 ? sa : sb);
+        const uint32_t ka = words[lva * 4 + (lane & 3)];
+        const uint32_t kb = sb < 0 ? 0u : words[lvb * 4 + (lane & 3)];
+        const uint32_t e[4] = {ka & 0xFFFFu, ka >> 16, kb & 0xFFFFu, kb >> 16};
+        uint32_t m[4], n = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            m[q] = __ballot_sync(0xFFFFFFFFu, e[q] >= t_floor);
+            n += __popc(m[q]);
+        }
+        uint32_t base = 0;
+        if (lane == 0 && n) base = atomicAdd(&sm.npend, n);
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (e[q] >= t_floor) {
+                const uint32_t slot = base + __popc(m[q] & lt);
+                const int32_t col = col_base + (q < 2 ? lva : lvb) * 8 + 2 * (lane & 3) + (q & 1);
+                if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(e[q], col);
+            }
+            base += __popc(m[q]);
+        }
+    }
+}
+
 __device__ __noinline__ void merge_pending(SmemCore &sm, const uint64_t *pend, int np, int k, int &run_i,
                                            int &out_i, int &run_len)
 {
@@ -806,6 +857,17 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 
 // ---------------------------------------------------------------- stream kernel
 
+// Programmatic dependent launch: the kernels are launched so that they may be
+// scheduled while the previous kernel on the stream is still finishing.  Each
+// waits here, before its first access to global memory, until that kernel has
+// completed and its writes are visible (a no-op when there is nothing to wait
+// for), then lets the next kernel on the stream be scheduled likewise.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Stream-plan ranges.  CTA b nominally starts at vector b * per of the
 // rows x vectors space; the start is moved to the nearest multiple of kThreads
 // vectors from its row's start, or to the row's end when less than kThreads
@@ -903,6 +965,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                    uint32_t *__restrict__ out_mask, uint64_t *__restrict__ partials,
                    uint32_t *__restrict__ tickets)
 {
+    grid_dependency_wait();
     extern __shared__ __align__(128) uint8_t dsmem[];
     uint4 *stages = reinterpret_cast<uint4 *>(dsmem);
     SmemCore &sm = *reinterpret_cast<SmemCore *>(dsmem + (size_t)kStages * kChunkVecs * 16);
@@ -1065,48 +1128,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                 t_floor = max(key_floor(t0), 1u);
                 if (t0 != 0) t_piece = t_floor;
             }
-            const bool hit = tmax >= t_floor;
-            if (hit) {
-#pragma unroll
-                for (int i = 0; i < kVecPerThread; ++i)
-                    st[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
-            }
-            __syncwarp();
-            {
-                // two spilled threads per step; one atomic reserves the step's slots
-                const int lane = tid & 31, warp = tid >> 5;
-                const uint32_t lt = (1u << lane) - 1u;
-                const uint32_t *words = reinterpret_cast<const uint32_t *>(st);
-                for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits;) {
-                    const int sa = __ffs(hits) - 1;
-                    hits &= hits - 1;
-                    const int sb = hits ? __ffs(hits) - 1 : -1;
-                    if (hits) hits &= hits - 1;
-                    const int lva = (lane >> 2) * kThreads + warp * 32 + sa;
-                    const int lvb = (lane >> 2) * kThreads + warp * 32 + (sb < 0 ? sa : sb);
-                    const uint32_t ka = words[lva * 4 + (lane & 3)];
-                    const uint32_t kb = sb < 0 ? 0u : words[lvb * 4 + (lane & 3)];
-                    const uint32_t e[4] = {ka & 0xFFFFu, ka >> 16, kb & 0xFFFFu, kb >> 16};
-                    uint32_t m[4], n = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        m[q] = __ballot_sync(0xFFFFFFFFu, e[q] >= t_floor);
-                        n += __popc(m[q]);
-                    }
-                    uint32_t base = 0;
-                    if (lane == 0 && n) base = atomicAdd(&sm.npend, n);
-                    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (e[q] >= t_floor) {
-                            const uint32_t slot = base + __popc(m[q] & lt);
-                            const int32_t col = col_base + (q < 2 ? lva : lvb) * 8 + 2 * (lane & 3) + (q & 1);
-                            if (slot < (uint32_t)kPendCap) pend[slot] = list_entry(e[q], col);
-                        }
-                        base += __popc(m[q]);
-                    }
-                }
-            }
+            push_pending(kv, tmax, t_floor, col_base, st, sm, pend);
             // the stage is next written by a bulk copy (async proxy)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             prev_lazy = true;
@@ -1215,6 +1237,7 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     const int span = (int)(blockIdx.x % S);
     const int64_t row = (int64_t)(blockIdx.x / S);
 
+    grid_dependency_wait();
     cluster_arrive_relaxed(); // paired with the wait before DSMEM use
 
     ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
@@ -1463,13 +1486,15 @@ cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, i
         cfg.blockDim = dim3(kThreads, 1, 1);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = S;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<S>, logits + r0 * row_stride, cols,
                                            row_stride, k, out_idx + r0 * k, out_val + r0 * k,
                                            out_count + r0, out_mask + r0);
@@ -1498,10 +1523,20 @@ int launch_stream(int dev, int sm_count, const uint16_t *logits, int64_t rows, i
             partials = s->partials;
             tickets = s->tickets;
         }
-        topk_stream_kernel<<<(unsigned)ctas, kThreads, kStreamSmemBytes, stream>>>(
-            logits + r0 * row_stride, (int32_t)cols, row_stride, k, nvr, nr * nvr, per, out_idx + r0 * k,
-            out_val + r0 * k, out_count + r0, out_mask + r0, partials, tickets);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kStreamSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_stream_kernel, logits + r0 * row_stride, (int32_t)cols,
+                                           row_stride, k, nvr, nr * nvr, per, out_idx + r0 * k, out_val + r0 * k,
+                                           out_count + r0, out_mask + r0, partials, tickets);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail_cuda(e);
     }
     return TF_TOPK_OK;
