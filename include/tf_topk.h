@@ -142,6 +142,45 @@ int32_t tf_topk_bf16_max_spans(void);     /* == TF_TOPK_MAX_SPANS */
 int32_t tf_topk_bf16_cta_threads(void);   /* threads per CTA */
 int32_t tf_topk_bf16_chunk_columns(void); /* columns one CTA holds in registers per pass */
 
+/* Most shard lists tf_topk_merge_bf16 merges per row. */
+#define TF_TOPK_MAX_SHARDS 64
+
+/*
+ * Merge of per-shard top lists into each row's top k: the pages' merge stage
+ * on its own (PR #713, change 3: span results merged in the same score /
+ * lower-index order), for rows whose columns were split over shards (a
+ * vocab-sharded head, or rows spread over several calls or devices).
+ *
+ *   in_idx, in_val, in_count, in_nonfinite_mask
+ *                      device; shard s, row r: in_idx[(s * rows + r) * k_in ..
+ *                      + k_in), likewise in_val, and in_count[s * rows + r],
+ *                      in_nonfinite_mask[s * rows + r] -- exactly what
+ *                      tf_topk_bf16 writes for one shard's column block
+ *                      (indices local to the block, best first).  Only the
+ *                      first min(k, k_in, in_count) entries of a list are read
+ *                      (no entry past them can reach the top k); a list ends
+ *                      early at an entry with a negative index or a NaN
+ *                      value.
+ *   rows, shards       1 <= shards <= TF_TOPK_MAX_SHARDS.
+ *   k_in               entries per input list, 1..TF_TOPK_MAX_K.
+ *   shard_offset       HOST array [shards]: the column of shard s's first
+ *                      column in the full row (0 <= offset < 2^31); global
+ *                      index = offset + local index.  Shards are meant to be
+ *                      disjoint column blocks.
+ *   k                  1..TF_TOPK_MAX_K; outputs as for tf_topk_bf16.
+ * The result is the top k of the union of the input entries under (score
+ * descending, lower global index first); its count is min(k, entries read);
+ * its mask is the OR of the shards' masks.  When every shard list holds its
+ * block's top k_in >= k, the result equals tf_topk_bf16 on the whole row.
+ * Asynchronous on `stream`; allocates nothing.  Returns a TF_TOPK_* status
+ * (ERR_SHAPE for a bad row/shard count or offset, ERR_K for k or k_in out of
+ * range, ERR_NULL, ERR_ALIGN as for tf_topk_bf16).
+ */
+int tf_topk_merge_bf16(const int32_t *in_idx, const uint16_t *in_val, const int32_t *in_count,
+                       const uint32_t *in_nonfinite_mask, int64_t rows, int32_t shards, int32_t k_in,
+                       const int64_t *shard_offset, int32_t k, int32_t *out_idx, uint16_t *out_val,
+                       int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream);
+
 /*
  * Allocation-free variant of the stream plan.
  *

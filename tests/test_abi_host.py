@@ -121,3 +121,30 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(topk, "LIBRARY", tmp_path / "missing.so")
     with pytest.raises(ImportError):
         topk.library()
+
+
+def merge_call(lib, rows=4, shards=2, k_in=8, offsets=(0, 100), k=8, in_idx=FAKE, in_val=FAKE, count=FAKE,
+               mask=FAKE, out_idx=FAKE, out_val=FAKE, out_count=FAKE, out_mask=FAKE):
+    from wide_bf16_row_gb300 import topk
+    return topk.tf_topk_merge_bf16(in_idx, in_val, count, mask, rows, shards, k_in, offsets, k, out_idx,
+                                   out_val, out_count, out_mask, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(k=0), 3), (dict(k=65), 3), (dict(k_in=0), 3), (dict(k_in=65), 3),
+    (dict(shards=0, offsets=(0,)), 2), (dict(shards=65, offsets=tuple(range(65))), 2), (dict(rows=-1), 2),
+    (dict(offsets=(0, -1)), 2), (dict(offsets=(0, 2**31)), 2),
+    (dict(in_idx=None), 1), (dict(in_val=None), 1), (dict(count=None), 1), (dict(mask=None), 1),
+    (dict(out_idx=None), 1), (dict(out_val=None), 1), (dict(out_count=None), 1), (dict(out_mask=None), 1),
+    (dict(offsets=None), 1),
+    (dict(in_idx=FAKE + 2), 4), (dict(in_val=FAKE + 1), 4), (dict(count=FAKE + 2), 4), (dict(mask=FAKE + 1), 4),
+    (dict(out_idx=FAKE + 2), 4), (dict(out_val=FAKE + 1), 4),
+])
+def test_merge_guards_reject_before_launch(lib, kwargs, status):
+    """tf_topk_merge_bf16 checks its arguments before any CUDA work."""
+    assert merge_call(lib, **kwargs) == status
+
+
+def test_merge_zero_rows_is_a_no_op(lib):
+    assert merge_call(lib, rows=0, in_idx=None, in_val=None, count=None, mask=None, out_idx=None,
+                      out_val=None, out_count=None, out_mask=None) == 0

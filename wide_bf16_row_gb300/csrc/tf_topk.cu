@@ -1302,6 +1302,101 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     write_row(row, fin, flen, flags, k, out_idx, out_val, out_count, out_mask);
 }
 
+// ---------------------------------------------------------------- shard-list merge kernel
+//
+// The merge stage on its own (TensorFold PR #713, change 3: span results are
+// merged "with the same tournament", i.e. in the same (score, lower index)
+// order).  Each of `shards` column blocks of a row has its own top list (as
+// tf_topk_bf16 writes it for that block: entries best first, a count, a
+// non-finite mask); the row's result is the top k of the union of those
+// entries, with every index moved by its shard's column offset.  One CTA per
+// row: each list's first min(k, count) entries become 64-bit entries (score,
+// ~global index, original bits), and an entry's rank is its position in its
+// own list plus, for every other list, the entries there that beat it (a
+// binary search, since every list is sorted the same way).
+
+constexpr int kMergeThreads = 128;
+
+// Order-preserving key of one bf16 value (0 for a NaN, which is never selected).
+__device__ __forceinline__ uint32_t merge_key(uint32_t raw)
+{
+    if ((raw & 0x7FFFu) > 0x7F80u) return 0;
+    return raw ^ ((raw & 0x8000u) ? 0xFFFFu : 0x8000u);
+}
+
+struct MergeShards {
+    int64_t offset[TF_TOPK_MAX_SHARDS];
+};
+
+__global__ void __launch_bounds__(kMergeThreads)
+topk_merge_kernel(const int32_t *__restrict__ in_idx, const uint16_t *__restrict__ in_val,
+                  const int32_t *__restrict__ in_count, const uint32_t *__restrict__ in_mask, int64_t rows,
+                  int32_t shards, int32_t k_in, MergeShards off, int32_t k, int32_t *__restrict__ out_idx,
+                  uint16_t *__restrict__ out_val, int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
+{
+    grid_dependency_wait();
+    __shared__ uint64_t lists[TF_TOPK_MAX_SHARDS][kMaxK];
+    __shared__ int32_t lens[TF_TOPK_MAX_SHARDS];
+    __shared__ uint32_t flags_all;
+    __shared__ int32_t total_all;
+    const int tid = threadIdx.x;
+    const int64_t r = blockIdx.x;
+    if (tid == 0) {
+        flags_all = 0;
+        total_all = 0;
+    }
+    __syncthreads();
+    // only an entry in a list's top min(k, k_in) can reach the row's top k
+    const int width = min(k, k_in);
+    for (int s = tid; s < shards; s += kMergeThreads) {
+        const int64_t cell = (int64_t)s * rows + r;
+        lens[s] = max(0, min(width, in_count[cell]));
+        atomicOr(&flags_all, in_mask[cell]);
+    }
+    __syncthreads();
+    // gather; an entry with no column or a NaN value ends its list
+    for (int t = tid; t < shards * width; t += kMergeThreads) {
+        const int s = t / width, p = t - s * width;
+        if (p >= lens[s]) continue;
+        const int64_t at = ((int64_t)s * rows + r) * k_in + p;
+        const int32_t li = in_idx[at];
+        const uint32_t key = merge_key(in_val[at]);
+        const int64_t gi = off.offset[s] + li;
+        if (li < 0 || key == 0 || gi > (int64_t)INT32_MAX) {
+            atomicMin(&lens[s], p);
+            continue;
+        }
+        lists[s][p] = list_entry(key, (int32_t)gi);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int sum = 0;
+        for (int s = 0; s < shards; ++s) sum += lens[s];
+        total_all = sum;
+    }
+    __syncthreads();
+    for (int t = tid; t < shards * width; t += kMergeThreads) {
+        const int s = t / width, p = t - s * width;
+        if (p >= lens[s]) continue;
+        const uint64_t x = lists[s][p];
+        int rank = 0;
+        for (int j = 0; j < shards && rank < k; ++j) rank += count_greater(lists[j], lens[j], x);
+        if (rank < k) {
+            out_idx[r * k + rank] = entry_col(x);
+            out_val[r * k + rank] = (uint16_t)(x & 0xFFFFu);
+        }
+    }
+    const int cnt = min(k, total_all);
+    for (int t = cnt + tid; t < k; t += kMergeThreads) {
+        out_idx[r * k + t] = -1;
+        out_val[r * k + t] = (uint16_t)kEmptyVal;
+    }
+    if (tid == 0) {
+        out_count[r] = cnt;
+        out_mask[r] = flags_all;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 constexpr size_t kStreamSmemBytes =
@@ -1634,6 +1729,54 @@ int run_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t row_stri
     return TF_TOPK_OK;
 }
 
+// tf_topk_merge_bf16: argument checks, then one CTA per row (in blocks of at
+// most 2^31 - 1 rows per launch).
+int run_merge(const int32_t *in_idx, const uint16_t *in_val, const int32_t *in_count, const uint32_t *in_mask,
+              int64_t rows, int32_t shards, int32_t k_in, const int64_t *shard_offset, int32_t k, int32_t *out_idx,
+              uint16_t *out_val, int32_t *out_count, uint32_t *out_mask, void *stream)
+{
+    if (k < 1 || k > kMaxK || k_in < 1 || k_in > kMaxK) return TF_TOPK_ERR_K;
+    if (rows < 0 || shards < 1 || shards > TF_TOPK_MAX_SHARDS) return TF_TOPK_ERR_SHAPE;
+    if (rows == 0) return TF_TOPK_OK;
+    if (!in_idx || !in_val || !in_count || !in_mask || !shard_offset || !out_idx || !out_val || !out_count ||
+        !out_mask)
+        return TF_TOPK_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(in_idx) & 3) || (reinterpret_cast<uintptr_t>(in_val) & 1) ||
+        (reinterpret_cast<uintptr_t>(in_count) & 3) || (reinterpret_cast<uintptr_t>(in_mask) & 3) ||
+        (reinterpret_cast<uintptr_t>(out_idx) & 3) || (reinterpret_cast<uintptr_t>(out_val) & 1) ||
+        (reinterpret_cast<uintptr_t>(out_count) & 3) || (reinterpret_cast<uintptr_t>(out_mask) & 3))
+        return TF_TOPK_ERR_ALIGN;
+    MergeShards off;
+    for (int s = 0; s < shards; ++s) {
+        if (shard_offset[s] < 0 || shard_offset[s] > (int64_t)INT32_MAX) return TF_TOPK_ERR_SHAPE;
+        off.offset[s] = shard_offset[s];
+    }
+    int dev = 0, sm_count = 0;
+    int st = device_setup(&dev, &sm_count);
+    if (st != TF_TOPK_OK) return st;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    const int64_t max_rows = (int64_t)INT32_MAX;
+    for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
+        const int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nr, 1, 1);
+        cfg.blockDim = dim3(kMergeThreads, 1, 1);
+        cfg.stream = strm;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // the row block's cells: shard s, row r at s * rows + r (k_in entries each)
+        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_merge_kernel, in_idx + r0 * k_in, in_val + r0 * k_in,
+                                           in_count + r0, in_mask + r0, rows, shards, k_in, off, k,
+                                           out_idx + r0 * k, out_val + r0 * k, out_count + r0, out_mask + r0);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TF_TOPK_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -1660,6 +1803,15 @@ int tf_topk_bf16_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t
 {
     return run_noalloc(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask,
                        stream);
+}
+
+int tf_topk_merge_bf16(const int32_t *in_idx, const uint16_t *in_val, const int32_t *in_count,
+                       const uint32_t *in_nonfinite_mask, int64_t rows, int32_t shards, int32_t k_in,
+                       const int64_t *shard_offset, int32_t k, int32_t *out_idx, uint16_t *out_val,
+                       int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream)
+{
+    return run_merge(in_idx, in_val, in_count, in_nonfinite_mask, rows, shards, k_in, shard_offset, k, out_idx,
+                     out_val, out_count, out_nonfinite_mask, stream);
 }
 
 int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)

@@ -44,6 +44,9 @@ def library() -> ctypes.CDLL:
         lib.tf_topk_bf16_with_plan.restype = ctypes.c_int
         lib.tf_topk_bf16_with_plan.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p,
                                                c_p, c_i32, c_p]
+        lib.tf_topk_merge_bf16.restype = ctypes.c_int
+        lib.tf_topk_merge_bf16.argtypes = [c_p, c_p, c_p, c_p, c_i64, c_i32, c_i32, c_p, c_i32, c_p, c_p, c_p,
+                                           c_p, c_p]
         lib.tf_topk_bf16_noalloc.restype = ctypes.c_int
         lib.tf_topk_bf16_noalloc.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
         lib.tf_topk_device_fault.restype = ctypes.c_int
@@ -109,6 +112,46 @@ def tf_topk_bf16_noalloc(logits: int, rows: int, cols: int, row_stride: int, k: 
     calls that overlap on the GPU race); returns the status code."""
     return library().tf_topk_bf16_noalloc(logits, rows, cols, row_stride, k, out_idx, out_val,
                                           out_count, out_nonfinite_mask, stream)
+
+
+def tf_topk_merge_bf16(in_idx: int, in_val: int, in_count: int, in_mask: int, rows: int, shards: int,
+                       k_in: int, shard_offset, k: int, out_idx: int, out_val: int, out_count: int,
+                       out_mask: int, stream: int | None) -> int:
+    """The C merge entry point; `shard_offset` is a host sequence of ints (or
+    None to pass NULL).  Returns the status code."""
+    off = None
+    if shard_offset is not None:
+        off = (ctypes.c_int64 * max(1, len(shard_offset)))(*[int(v) for v in shard_offset])
+    return library().tf_topk_merge_bf16(in_idx, in_val, in_count, in_mask, rows, shards, k_in, off, k,
+                                        out_idx, out_val, out_count, out_mask, stream)
+
+
+def merge_bf16(idx, val, count, mask, offsets, k: int, *, out=None, stream=None):
+    """Merge per-shard top lists into each row's top k.
+
+    idx int32 [shards, rows, k_in], val bf16/int16/uint16 [shards, rows, k_in],
+    count int32 [shards, rows], mask int32/uint32 [shards, rows] (all CUDA,
+    contiguous), offsets: the column offset of each shard (host ints).
+    Returns (idx int32 [rows, k], val [rows, k], count int32 [rows], mask int32 [rows]).
+    """
+    import torch
+
+    shards, rows, k_in = idx.shape
+    for t in (idx, val, count, mask):
+        if not t.is_cuda or not t.is_contiguous():
+            raise TopkError(ERR_SHAPE, "merge inputs must be contiguous CUDA tensors")
+    if out is None:
+        dev = idx.device
+        out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
+               torch.empty((rows, k), dtype=val.dtype, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev))
+    if stream is None:
+        stream = torch.cuda.current_stream(idx.device)
+    _check(tf_topk_merge_bf16(idx.data_ptr(), val.data_ptr(), count.data_ptr(), mask.data_ptr(), rows, shards,
+                              k_in, list(offsets), k, out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+                              out[3].data_ptr(), stream.cuda_stream))
+    return out
 
 
 def device_fault() -> int:
