@@ -146,6 +146,13 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
     return d;
 }
 
+__device__ __forceinline__ uint32_t max_s16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b)
 {
     uint32_t d;
@@ -475,6 +482,37 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
 // Selection for one chunk whose keys are in kv (see chunk_keys) with this
 // thread's max key tmax: the row piece's running list (run_i, run_len)
 // absorbs the chunk's top-k.  Block-uniform: every thread calls it.
+// Max key of this thread's raw bf16 words without turning them into keys.
+// Signed 16-bit order is score order among non-negative values, so the signed
+// max gives the best non-negative score (key = raw + 0x8000); the signed max
+// also shows a +inf/+NaN (>= 0x7F80) and the unsigned max a -inf/-NaN
+// (>= 0xFF80).  Returns false -- the keys are needed -- when the thread holds
+// any of those or no non-negative value at all.
+__device__ __forceinline__ bool raw_tmax(const uint32_t (&kv)[kVecPerThread][4], uint32_t &tmax)
+{
+    uint32_t smx = 0x80008000u, umx = 0;
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            smx = max_s16x2(smx, kv[i][w]);
+            umx = max_u16x2(umx, kv[i][w]);
+        }
+    const int32_t smax = max((int32_t)(int16_t)(smx & 0xFFFFu), (int32_t)(int16_t)(smx >> 16));
+    const uint32_t umax = max(umx & 0xFFFFu, umx >> 16);
+    if (smax < 0 || smax >= (int32_t)0x7F80 || umax >= 0xFF80u) return false;
+    tmax = (uint32_t)smax + 0x8000u;
+    return true;
+}
+
+__device__ __forceinline__ void keys_in_place(uint32_t (&kv)[kVecPerThread][4])
+{
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) kv[i][w] = keys_from_raw2(kv[i][w]);
+}
+
 // Prefilter bound of one chunk (block-uniform, one barrier).  The fw warps
 // whose 32 lanes all hold data each find the j-th largest of their lanes'
 // maxima, j = ceil(k / fw); the minimum t0 over them is reached by at least
@@ -511,8 +549,8 @@ __device__ __forceinline__ uint32_t prefilter_bound(uint32_t tmax, int nvalid, i
     return t0;
 }
 
-__device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, int nvalid,
-                                             int32_t col_base, int k, SmemCore &sm, uint4 *stage,
+__device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, bool raw,
+                                             int nvalid, int32_t col_base, int k, SmemCore &sm, uint4 *stage,
                                              int &run_i, int &chunk_i, int &free_i, int &run_len)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -530,6 +568,8 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
     //      such thread spills its keys, and its warp scans them one word per lane
     const bool hit = tmax >= t_floor;
     if (hit) {
+        if (raw) keys_in_place(kv);
+        raw = false;
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i)
             stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
@@ -552,6 +592,7 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
     if (n > (uint32_t)kCandCap) {
         // heavy ties: stage every key in column order (below t_floor -> 0) and
         // select exactly
+        if (raw) keys_in_place(kv);
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i) {
             uint32_t q[4];
@@ -1274,8 +1315,12 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
             kv[i][2] = q.z;
             kv[i][3] = q.w;
         }
-        const uint32_t tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
-        select_chunk(kv, tmax, nvalid, col_base, k, sm, keys, run_i, chunk_i, free_i, run_len);
+        // a full chunk inside the row: the max from the raw bits where it can be
+        const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && geo.cend <= geo.vfull1;
+        uint32_t tmax = 0;
+        const bool raw = full && raw_tmax(kv, tmax);
+        if (!raw) tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+        select_chunk(kv, tmax, raw, nvalid, col_base, k, sm, keys, run_i, chunk_i, free_i, run_len);
         __syncthreads(); // the running list is read by the next chunk's threshold
     }
 
