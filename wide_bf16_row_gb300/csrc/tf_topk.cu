@@ -1300,23 +1300,34 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         geo.cend = min(v_end, cbeg + kChunkVecs);
         const int nvalid = geo.cend - cbeg;
         const int32_t col_base = cbeg * 8 - geo.m;
+        const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && geo.cend <= geo.vfull1;
         uint32_t kv[kVecPerThread][4];
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            const int lv = i * kThreads + tid;
-            uint4 q = make_uint4(0, 0, 0, 0);
-            if (lv < nvalid) {
-                const int32_t v = cbeg + lv;
-                q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
-                                                       : load_edge_vector(geo.rowp, cols, geo.m, v);
+            for (int i = 0; i < kVecPerThread; ++i) {
+                const uint4 q = ld_stream(vbase + cbeg + i * kThreads + tid);
+                kv[i][0] = q.x;
+                kv[i][1] = q.y;
+                kv[i][2] = q.z;
+                kv[i][3] = q.w;
             }
-            kv[i][0] = q.x;
-            kv[i][1] = q.y;
-            kv[i][2] = q.z;
-            kv[i][3] = q.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) {
+                const int lv = i * kThreads + tid;
+                uint4 q = make_uint4(0, 0, 0, 0);
+                if (lv < nvalid) {
+                    const int32_t v = cbeg + lv;
+                    q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
+                                                           : load_edge_vector(geo.rowp, cols, geo.m, v);
+                }
+                kv[i][0] = q.x;
+                kv[i][1] = q.y;
+                kv[i][2] = q.z;
+                kv[i][3] = q.w;
+            }
         }
         // a full chunk inside the row: the max from the raw bits where it can be
-        const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && geo.cend <= geo.vfull1;
         uint32_t tmax = 0;
         const bool raw = full && raw_tmax(kv, tmax);
         if (!raw) tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
