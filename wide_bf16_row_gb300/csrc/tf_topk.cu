@@ -583,9 +583,6 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
         if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local);
         if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1);
     }
-    // this thread's stage slots may have been written (exact key pass, spill);
-    // the stage is next written by a bulk copy (async proxy)
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     uint32_t n = sm.n_cand;
     if (n == 0) return; // nothing reaches the threshold: the running list stands
@@ -603,7 +600,6 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
             }
             stage[i * kThreads + tid] = make_uint4(q[0], q[1], q[2], q[3]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
         n = sm.n_cand; // == k
