@@ -1327,9 +1327,15 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         uint32_t tmax = 0;
         const bool raw = full && raw_tmax(kv, tmax);
         if (!raw) tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+        // The previous chunk's merge must be complete before its bound is read.
+        // With two spans the barrier sits here, so the loads and keys above
+        // overlap the slowest threads' merge; with more spans (shorter spans,
+        // measured) it closes each chunk.
+        if constexpr (S == 2) __syncthreads();
         select_chunk(kv, tmax, raw, nvalid, col_base, k, sm, keys, run_i, chunk_i, free_i, run_len);
-        __syncthreads(); // the running list is read by the next chunk's threshold
+        if constexpr (S != 2) __syncthreads();
     }
+    __syncthreads(); // the last merge is complete
 
     // ---- push this span's list into the leader's shared memory
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); // every CTA has started
