@@ -1,0 +1,86 @@
+"""CPU oracle for the nucleus (top-p) step after the top-k -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/`` may import this module; the product path never does.
+
+Source: the pull request page "qwen27 metal: restore the long-copy driver for
+a lone greedy stream on M5 (#3013) - #3069" (TensorFold), section "Receipt":
+drafted streams are sampled at temperature 0.7 with top-k 20 and top-p 0.95.
+The pages name the settings but not the procedure; the reading taken here is
+the usual one, top-k first and then top-p:
+
+  * a row's candidates are its top-k entries (best first, ``count`` of them);
+  * at temperature T > 0 their probabilities are the softmax of value / T over
+    those entries alone;
+  * the kept prefix is the shortest one whose probabilities sum to at least
+    top_p (at least one entry); top_p == 1 keeps every entry;
+  * the kept entries' probabilities are renormalised to sum to 1, the others
+    are 0;
+  * T == 0 is greedy: the first entry alone, probability 1;
+  * an infinite best value (+inf, or -inf when every entry is -inf) gives the
+    entries equal to it equal shares and every other entry 0.
+
+Everything is computed in float64 with a plain sequential sum.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def bf16_value(bits: int) -> float:
+    """The real value of bf16 bits (exact)."""
+    return float(np.array([int(bits) << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def nucleus_row(vals: list[float], temperature: float, top_p: float) -> tuple[list[float], int, list[float]]:
+    """One row: (probabilities of every entry, kept count, renormalised kept
+    probabilities padded with zeros)."""
+    n = len(vals)
+    if n == 0:
+        return [], 0, []
+    if temperature == 0.0:
+        p = [1.0] + [0.0] * (n - 1)
+        return p, 1, list(p)
+    top = vals[0]
+    if math.isinf(top):
+        share = [1.0 if v == top else 0.0 for v in vals]
+        total = sum(share)
+        p = [s / total for s in share]
+    else:
+        e = [math.exp((v - top) / temperature) for v in vals]
+        total = 0.0
+        for x in e:
+            total += x
+        p = [x / total for x in e]
+    if top_p >= 1.0:
+        keep = n
+    else:
+        keep, acc = n, 0.0
+        for i, x in enumerate(p):
+            acc += x
+            if acc >= top_p:
+                keep = i + 1
+                break
+    kept = 0.0
+    for x in p[:keep]:
+        kept += x
+    out = [x / kept for x in p[:keep]] + [0.0] * (n - keep)
+    return p, keep, out
+
+
+def nucleus(val_bits: np.ndarray, count: np.ndarray, temperature: float, top_p: float):
+    """Rows of top-k results -> (prob float64 [rows][k], keep int [rows], and
+    the pre-truncation softmax float64 [rows][k])."""
+    rows, k = val_bits.shape
+    prob = np.zeros((rows, k))
+    soft = np.zeros((rows, k))
+    keep = np.zeros(rows, dtype=np.int64)
+    for r in range(rows):
+        n = int(count[r])
+        vals = [bf16_value(b) for b in val_bits[r, :n]]
+        p, m, out = nucleus_row(vals, temperature, top_p)
+        soft[r, :n] = p
+        prob[r, :n] = out
+        keep[r] = m
+    return prob, keep, soft
