@@ -17,7 +17,10 @@ the usual one, top-k first and then top-p:
     are 0;
   * T == 0 is greedy: the first entry alone, probability 1;
   * an infinite best value (+inf, or -inf when every entry is -inf) gives the
-    entries equal to it equal shares and every other entry 0.
+    entries equal to it equal shares and every other entry 0;
+  * NaN is not a score: the top-k ranks it below every number, so NaN entries
+    form the tail of a row and take no probability; a row of NaN alone keeps
+    nothing (keep 0, all probabilities 0).
 
 Everything is computed in float64 with a plain sequential sum.
 """
@@ -36,7 +39,12 @@ def bf16_value(bits: int) -> float:
 def nucleus_row(vals: list[float], temperature: float, top_p: float) -> tuple[list[float], int, list[float]]:
     """One row: (probabilities of every entry, kept count, renormalised kept
     probabilities padded with zeros)."""
-    n = len(vals)
+    size = len(vals)
+    n = next((i for i, v in enumerate(vals) if math.isnan(v)), size)
+    if n < size:
+        p, keep, out = nucleus_row(vals[:n], temperature, top_p)
+        pad = [0.0] * (size - n)
+        return p + pad, keep, out + pad
     if n == 0:
         return [], 0, []
     if temperature == 0.0:

@@ -83,3 +83,11 @@ def test_rows_entry_point_keeps_the_untruncated_softmax():
     prob, keep, soft = nucleus(bits, np.array([4]), 0.7, 0.5)
     assert keep.tolist() == [2]
     assert soft[0].tolist() == [0.25] * 4 and prob[0].tolist() == [0.5, 0.5, 0.0, 0.0]
+
+
+def test_nan_entries_take_no_probability():
+    nan = math.nan
+    p, keep, out = nucleus_row([2.0, 2.0, nan], 0.7, 0.9)
+    assert p == [0.5, 0.5, 0.0] and keep == 2 and out == [0.5, 0.5, 0.0]
+    assert nucleus_row([nan, nan], 0.7, 0.9) == ([0.0, 0.0], 0, [0.0, 0.0])
+    assert nucleus_row([nan], 0.0, 0.9) == ([0.0], 0, [0.0])
