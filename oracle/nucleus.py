@@ -36,13 +36,16 @@ def bf16_value(bits: int) -> float:
     return float(np.array([int(bits) << 16], dtype=np.uint32).view(np.float32)[0])
 
 
-def nucleus_row(vals: list[float], temperature: float, top_p: float) -> tuple[list[float], int, list[float]]:
+def nucleus_row(vals: list[float], temperature: float, top_p: float,
+                keep: int | None = None) -> tuple[list[float], int, list[float]]:
     """One row: (probabilities of every entry, kept count, renormalised kept
-    probabilities padded with zeros)."""
+    probabilities padded with zeros).  ``keep``, when given, fixes the kept
+    count in place of the top-p cut (a caller comparing a result whose cut
+    fell on the other side of a rounding boundary)."""
     size = len(vals)
     n = next((i for i, v in enumerate(vals) if math.isnan(v)), size)
     if n < size:
-        p, keep, out = nucleus_row(vals[:n], temperature, top_p)
+        p, keep, out = nucleus_row(vals[:n], temperature, top_p, keep)
         pad = [0.0] * (size - n)
         return p + pad, keep, out + pad
     if n == 0:
@@ -50,30 +53,35 @@ def nucleus_row(vals: list[float], temperature: float, top_p: float) -> tuple[li
     if temperature == 0.0:
         p = [1.0] + [0.0] * (n - 1)
         return p, 1, list(p)
+    # unnormalised weights w: the probabilities are w / sum(w)
     top = vals[0]
     if math.isinf(top):
-        share = [1.0 if v == top else 0.0 for v in vals]
-        total = sum(share)
-        p = [s / total for s in share]
+        w = [1.0 if v == top else 0.0 for v in vals]
     else:
-        e = [math.exp((v - top) / temperature) for v in vals]
-        total = 0.0
-        for x in e:
-            total += x
-        p = [x / total for x in e]
-    if top_p >= 1.0:
+        w = [math.exp((v - top) / temperature) for v in vals]
+    total = 0.0
+    for x in w:
+        total += x
+    p = [x / total for x in w]
+    # the cut: the shortest prefix whose probabilities reach top_p, i.e. whose
+    # weights reach top_p * total (compared on the weights, so a prefix that
+    # reaches top_p exactly -- equal shares -- is decided without the
+    # rounding of the division)
+    if keep is not None:
+        keep = max(0, min(int(keep), n))
+    elif top_p >= 1.0:
         keep = n
     else:
-        keep, acc = n, 0.0
-        for i, x in enumerate(p):
+        keep, acc, need = n, 0.0, top_p * total
+        for i, x in enumerate(w):
             acc += x
-            if acc >= top_p:
+            if acc >= need:
                 keep = i + 1
                 break
     kept = 0.0
-    for x in p[:keep]:
+    for x in w[:keep]:
         kept += x
-    out = [x / kept for x in p[:keep]] + [0.0] * (n - keep)
+    out = [x / kept for x in w[:keep]] + [0.0] * (n - keep) if keep else [0.0] * n
     return p, keep, out
 
 
@@ -85,7 +93,7 @@ def nucleus(val_bits: np.ndarray, count: np.ndarray, temperature: float, top_p: 
     soft = np.zeros((rows, k))
     keep = np.zeros(rows, dtype=np.int64)
     for r in range(rows):
-        n = int(count[r])
+        n = max(0, min(k, int(count[r])))     # a list holds at most k entries
         vals = [bf16_value(b) for b in val_bits[r, :n]]
         p, m, out = nucleus_row(vals, temperature, top_p)
         soft[r, :n] = p

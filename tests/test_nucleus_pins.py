@@ -91,3 +91,12 @@ def test_nan_entries_take_no_probability():
     assert p == [0.5, 0.5, 0.0] and keep == 2 and out == [0.5, 0.5, 0.0]
     assert nucleus_row([nan, nan], 0.7, 0.9) == ([0.0, 0.0], 0, [0.0, 0.0])
     assert nucleus_row([nan], 0.0, 0.9) == ([0.0], 0, [0.0])
+
+
+def test_a_fixed_keep_replaces_the_cut():
+    p, keep, out = nucleus_row([1.0, 1.0, 1.0, 1.0], 0.7, 0.3, keep=3)
+    assert keep == 3 and out == pytest.approx([1 / 3, 1 / 3, 1 / 3, 0.0])
+    for top_p in (0.2, 0.6, 0.97):   # fixing the cut the rule would take changes nothing
+        vals = [2.5, 1.0, 0.25, -3.0]
+        ref = nucleus_row(vals, 0.7, top_p)
+        assert nucleus_row(vals, 0.7, 0.5, keep=ref[1]) == ref
