@@ -216,6 +216,40 @@ int tf_topk_bf16_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t
                          int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
                          uint32_t *out_nonfinite_mask, void *stream);
 
+/*
+ * Sampling probabilities over each row's top-k list (nucleus / top-p).
+ *
+ * The speculative decoding receipts of the TensorFold PR #3069 page
+ * ("Receipt") sample draft streams at temperature 0.7 with top-k 20 and top-p
+ * 0.95.  The page names those settings, not the procedure; this call takes
+ * the usual one, top-k first and then top-p:
+ *   - the entries of row r are the first min(k, count[r]) of its list, cut
+ *     before the first NaN value (the top-k ranks NaN below every number);
+ *   - with T > 0 their probabilities are the softmax of value / T over those
+ *     entries alone (computed in fp32, relative to the best value); T == 0
+ *     is greedy (the first entry alone); an infinite best value gives the
+ *     entries equal to it equal shares;
+ *   - keep[r] is the length of the shortest best-first prefix whose mass
+ *     reaches top_p (every entry when top_p == 1), and out_prob holds that
+ *     prefix renormalised to sum 1, then zeros.
+ *
+ *   val, count         device: val[r * k + i] bf16 bits and count[r], exactly
+ *                      as tf_topk_bf16 (or tf_topk_merge_bf16) writes them.
+ *   rows, k            rows >= 0; k 1..TF_TOPK_MAX_K (the lists' length).
+ *   temperature        finite, >= 0.
+ *   top_p              0 < top_p <= 1.
+ *   out_prob           device float [rows][k], row-major.
+ *   out_keep           device int32 [rows]; 0 for a row with no number.
+ * Asynchronous on `stream`; allocates nothing; launched as a programmatic
+ * dependent of the call before it on the stream, so queued right after
+ * tf_topk_bf16 it starts as that call's last CTAs finish.  Returns a
+ * TF_TOPK_* status (ERR_ARG for temperature or top_p, ERR_K, ERR_SHAPE for
+ * rows < 0, ERR_NULL, ERR_ALIGN: val 2-byte, the others 4-byte aligned).
+ */
+#define TF_TOPK_ERR_ARG 9 /* tf_topk_nucleus_bf16: temperature or top_p out of range */
+int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature,
+                         float top_p, float *out_prob, int32_t *out_keep, void *stream);
+
 /* Human-readable text for a TF_TOPK_* status (static storage). */
 const char *tf_topk_strerror(int status);
 

@@ -99,8 +99,8 @@ def test_zero_rows_is_a_no_op(lib):
 
 def test_strerror_covers_every_status(lib):
     from wide_bf16_row_gb300 import topk
-    texts = {topk.strerror(s) for s in range(8)}
-    assert len(texts) == 8 and "unknown status" not in texts
+    texts = {topk.strerror(s) for s in range(10)}
+    assert len(texts) == 10 and "unknown status" not in texts
     assert topk.strerror(99) == "unknown status"
 
 
@@ -148,3 +148,25 @@ def test_merge_guards_reject_before_launch(lib, kwargs, status):
 def test_merge_zero_rows_is_a_no_op(lib):
     assert merge_call(lib, rows=0, in_idx=None, in_val=None, count=None, mask=None, out_idx=None,
                       out_val=None, out_count=None, out_mask=None) == 0
+
+
+def nucleus_call(lib, rows=4, k=8, temperature=0.7, top_p=0.95, val=FAKE, count=FAKE, prob=FAKE, keep=FAKE):
+    from wide_bf16_row_gb300 import topk
+    return topk.tf_topk_nucleus_bf16(val, count, rows, k, temperature, top_p, prob, keep, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(temperature=-0.5), 9), (dict(temperature=float("nan")), 9), (dict(temperature=float("inf")), 9),
+    (dict(top_p=0.0), 9), (dict(top_p=-1.0), 9), (dict(top_p=1.5), 9), (dict(top_p=float("nan")), 9),
+    (dict(k=0), 3), (dict(k=65), 3), (dict(rows=-1), 2),
+    (dict(val=None), 1), (dict(count=None), 1), (dict(prob=None), 1), (dict(keep=None), 1),
+    (dict(val=FAKE + 1), 4), (dict(count=FAKE + 2), 4), (dict(prob=FAKE + 2), 4), (dict(keep=FAKE + 1), 4),
+])
+def test_nucleus_guards_reject_before_launch(lib, kwargs, status):
+    """tf_topk_nucleus_bf16 checks its arguments before any CUDA work."""
+    assert nucleus_call(lib, **kwargs) == status
+
+
+def test_nucleus_zero_rows_is_a_no_op(lib):
+    assert nucleus_call(lib, rows=0, val=None, count=None, prob=None, keep=None) == 0
+    assert nucleus_call(lib, rows=0, temperature=0.0, top_p=1.0) == 0

@@ -53,6 +53,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include <map>
 #include <mutex>
 #include <thread>
@@ -1455,6 +1457,88 @@ topk_merge_kernel(const int32_t *__restrict__ in_idx, const uint16_t *__restrict
     }
 }
 
+// ------------------------------------------------ nucleus (top-p) after the top-k
+//
+// Sampling probabilities over each row's top-k list, as the speculative
+// decoding receipts of the TensorFold PR #3069 page ("Receipt": temperature
+// 0.7, top-k 20, top-p 0.95) use them: the softmax of value / T over the
+// row's entries, the shortest best-first prefix whose mass reaches top_p, that
+// prefix renormalised.  One warp per row (k <= 64: two entries a lane); the
+// prefix mass is a warp scan, the cut a ballot.
+
+constexpr int kNucleusWarps = 8;
+
+__device__ __forceinline__ float warp_inclusive_scan(float x, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+__global__ void __launch_bounds__(kNucleusWarps * 32)
+topk_nucleus_kernel(const uint16_t *__restrict__ val, const int32_t *__restrict__ count, int64_t rows, int32_t k,
+                    float temperature, float top_p, float *__restrict__ out_prob, int32_t *__restrict__ out_keep)
+{
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * kNucleusWarps + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const int n_in = max(0, min((int)k, count[r]));
+    float v[2];
+    bool nan[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        v[j] = i < n_in ? __uint_as_float((uint32_t)val[r * k + i] << 16) : 0.f;
+        nan[j] = i < n_in && isnan(v[j]);
+    }
+    // the top-k ranks NaN below every number: the numbers are the prefix before the first NaN
+    const unsigned nan_lo = __ballot_sync(0xFFFFFFFFu, nan[0]);
+    const unsigned nan_hi = __ballot_sync(0xFFFFFFFFu, nan[1]);
+    const int n = nan_lo ? __ffs(nan_lo) - 1 : (nan_hi ? 31 + __ffs(nan_hi) : n_in);
+    const float best = __shfl_sync(0xFFFFFFFFu, v[0], 0);
+    float e[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        if (i >= n)
+            e[j] = 0.f;
+        else if (temperature == 0.f)
+            e[j] = i == 0 ? 1.f : 0.f;            // greedy
+        else if (isinf(best))
+            e[j] = v[j] == best ? 1.f : 0.f;      // equal shares among the infinite best
+        else
+            e[j] = expf((v[j] - best) / temperature);
+    }
+    // running mass, best first: positions 0..31 then 32..63
+    const float c_lo = warp_inclusive_scan(e[0], lane);
+    const float c_hi = warp_inclusive_scan(e[1], lane) + __shfl_sync(0xFFFFFFFFu, c_lo, 31);
+    const float total = __shfl_sync(0xFFFFFFFFu, c_hi, 31);
+    int keep = n;
+    if (top_p < 1.f && n > 0) {
+        // mass c reaches top_p of the total when c - top_p * total >= 0; one
+        // fused multiply-add rounds that difference once, which keeps its
+        // sign, so the comparison is exact (equal shares cut exactly)
+        const unsigned hit_lo = __ballot_sync(0xFFFFFFFFu, lane < n && fmaf(-top_p, total, c_lo) >= 0.f);
+        const unsigned hit_hi = __ballot_sync(0xFFFFFFFFu, lane + 32 < n && fmaf(-top_p, total, c_hi) >= 0.f);
+        keep = hit_lo ? __ffs(hit_lo) : (hit_hi ? 32 + __ffs(hit_hi) : n);
+    }
+    // mass of the kept prefix (position keep - 1 of the scan)
+    const int last = max(keep, 1) - 1;
+    const float kept_lo = __shfl_sync(0xFFFFFFFFu, c_lo, last & 31);
+    const float kept_hi = __shfl_sync(0xFFFFFFFFu, c_hi, last & 31);
+    const float kept = last < 32 ? kept_lo : kept_hi;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        if (i < k) out_prob[r * k + i] = i < keep ? e[j] / kept : 0.f;
+    }
+    if (lane == 0) out_keep[r] = keep;
+}
+
 // ---------------------------------------------------------------- host side
 
 constexpr size_t kStreamSmemBytes =
@@ -1835,6 +1919,42 @@ int run_merge(const int32_t *in_idx, const uint16_t *in_val, const int32_t *in_c
     return TF_TOPK_OK;
 }
 
+// tf_topk_nucleus_bf16: argument checks, then one warp per row.
+int run_nucleus(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature, float top_p,
+                float *out_prob, int32_t *out_keep, void *stream)
+{
+    if (k < 1 || k > kMaxK) return TF_TOPK_ERR_K;
+    if (rows < 0) return TF_TOPK_ERR_SHAPE;
+    if (!(temperature >= 0.f) || std::isinf(temperature) || !(top_p > 0.f && top_p <= 1.f)) return TF_TOPK_ERR_ARG;
+    if (rows == 0) return TF_TOPK_OK;
+    if (!val || !count || !out_prob || !out_keep) return TF_TOPK_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(val) & 1) || (reinterpret_cast<uintptr_t>(count) & 3) ||
+        (reinterpret_cast<uintptr_t>(out_prob) & 3) || (reinterpret_cast<uintptr_t>(out_keep) & 3))
+        return TF_TOPK_ERR_ALIGN;
+    int dev = 0, sm_count = 0;
+    int st = device_setup(&dev, &sm_count);
+    if (st != TF_TOPK_OK) return st;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    const int64_t max_rows = (int64_t)INT32_MAX * kNucleusWarps;
+    for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
+        const int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((nr + kNucleusWarps - 1) / kNucleusWarps), 1, 1);
+        cfg.blockDim = dim3(kNucleusWarps * 32, 1, 1);
+        cfg.stream = strm;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_nucleus_kernel, val + r0 * k, count + r0, nr, k, temperature,
+                                           top_p, out_prob + r0 * k, out_keep + r0);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TF_TOPK_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -1870,6 +1990,12 @@ int tf_topk_merge_bf16(const int32_t *in_idx, const uint16_t *in_val, const int3
 {
     return run_merge(in_idx, in_val, in_count, in_nonfinite_mask, rows, shards, k_in, shard_offset, k, out_idx,
                      out_val, out_count, out_nonfinite_mask, stream);
+}
+
+int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature,
+                         float top_p, float *out_prob, int32_t *out_keep, void *stream)
+{
+    return run_nucleus(val, count, rows, k, temperature, top_p, out_prob, out_keep, stream);
 }
 
 int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)
@@ -1920,6 +2046,7 @@ const char *tf_topk_strerror(int status)
     case TF_TOPK_ERR_PLAN: return "unknown plan code";
     case TF_TOPK_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
     case TF_TOPK_ERR_CUDA: return "CUDA runtime error (see tf_topk_last_cuda_error)";
+    case TF_TOPK_ERR_ARG: return "temperature or top_p out of range";
     case TF_TOPK_ERR_SCRATCH: return "the launch needs more scratch slots than the static area of "
                                      "tf_topk_bf16_noalloc holds (TF_TOPK_NOALLOC_MAX_CTAS)";
     default: return "unknown status";

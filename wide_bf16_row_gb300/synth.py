@@ -203,3 +203,47 @@ def mixed_rows(rows: int, cols: int, seed: int, row_stride: int | None = None,
             vals[r, pos] = extra[rng.integers(0, len(extra), size=n)]
     stride = cols if row_stride is None else row_stride
     return _pad(rng, vals, stride)
+
+
+def ranked_lists(rows: int, k: int, seed: int) -> tuple[np.ndarray, np.ndarray]:
+    """Lists shaped like a top-k's output, for the step that consumes them:
+    ``(val uint16 [rows, k], count int32 [rows])``, each row's first ``count``
+    entries best first with NaN last, the slots past ``count`` garbage bits.
+
+    Row kinds cycle through: normal values at several spreads, heavy ties,
+    one or more +inf at the head, all -inf, -inf after numbers, NaN tails,
+    all NaN, empty, and spreads wide enough that exp(value / T) underflows.
+    """
+    rng = np.random.default_rng(seed)
+    val = rng.integers(0, 1 << 16, size=(rows, k), dtype=np.uint16)
+    count = np.empty(rows, np.int32)
+    kinds = 10
+    for r in range(rows):
+        kind = r % kinds
+        n = k if rng.random() < 0.6 else int(rng.integers(0, k + 1))
+        sigma = float(rng.choice([0.05, 0.25, 1.0, 4.0, 16.0]))
+        z = rng.standard_normal(n).astype(np.float32) * np.float32(sigma)
+        if kind == 1:                                   # heavy ties
+            z = rng.choice(np.float32([0.5, 0.0, -1.25]), size=n)
+        elif kind == 8:                                 # underflowing tail
+            z = rng.uniform(-300.0, 3.0, size=n).astype(np.float32)
+        bits = round_to_bf16(z)
+        if kind == 2 and n:                             # +inf at the head
+            bits[: int(rng.integers(1, n + 1))] = BF16_POS_INF
+        elif kind == 3:                                 # nothing but -inf
+            bits[:] = BF16_NEG_INF
+        elif kind == 4 and n:                           # -inf after some numbers
+            bits[int(rng.integers(0, n)):] = BF16_NEG_INF
+        nan_tail = 0
+        if kind == 5 and n:
+            nan_tail = int(rng.integers(1, n + 1))
+        elif kind == 6:
+            nan_tail = n
+        elif kind == 7:
+            n = 0
+        body = bits[: n - nan_tail]
+        order = np.argsort(-bf16_to_float(body), kind="stable")
+        val[r, : n - nan_tail] = body[order]
+        val[r, n - nan_tail: n] = _nan_bits(rng, nan_tail)
+        count[r] = n
+    return val, count

@@ -15,6 +15,7 @@ LIBRARY = PKG / "libtf_topk.so"
 # status codes (include/tf_topk.h)
 OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_PLAN, ERR_DEVICE, ERR_CUDA = range(8)
 ERR_SCRATCH = 8  # tf_topk_bf16_noalloc only
+ERR_ARG = 9  # tf_topk_nucleus_bf16 only
 
 # launch plans (include/tf_topk.h)
 PLAN_AUTO, PLAN_SINGLE, PLAN_STREAM = 0, 1, 32
@@ -49,6 +50,8 @@ def library() -> ctypes.CDLL:
                                            c_p, c_p]
         lib.tf_topk_bf16_noalloc.restype = ctypes.c_int
         lib.tf_topk_bf16_noalloc.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
+        lib.tf_topk_nucleus_bf16.restype = ctypes.c_int
+        lib.tf_topk_nucleus_bf16.argtypes = [c_p, c_p, c_i64, c_i32, ctypes.c_float, ctypes.c_float, c_p, c_p, c_p]
         lib.tf_topk_device_fault.restype = ctypes.c_int
         lib.tf_topk_device_fault.argtypes = []
         lib.tf_topk_bf16_plan.restype = c_i32
@@ -151,6 +154,38 @@ def merge_bf16(idx, val, count, mask, offsets, k: int, *, out=None, stream=None)
     _check(tf_topk_merge_bf16(idx.data_ptr(), val.data_ptr(), count.data_ptr(), mask.data_ptr(), rows, shards,
                               k_in, list(offsets), k, out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
                               out[3].data_ptr(), stream.cuda_stream))
+    return out
+
+
+def tf_topk_nucleus_bf16(val: int, count: int, rows: int, k: int, temperature: float, top_p: float,
+                         out_prob: int, out_keep: int, stream: int | None) -> int:
+    """The C nucleus (top-p) entry point with raw pointers; returns the status code."""
+    return library().tf_topk_nucleus_bf16(val, count, rows, k, temperature, top_p, out_prob, out_keep, stream)
+
+
+def nucleus_bf16(val, count, temperature: float, top_p: float, *, out=None, stream=None):
+    """Sampling probabilities over top-k lists (softmax of value / T, then the
+    shortest best-first prefix with mass >= top_p, renormalised).
+
+    val bf16/int16/uint16 [rows, k] and count int32 [rows] as ``topk_bf16``
+    returns them (contiguous CUDA tensors).  Returns (prob float32 [rows, k],
+    keep int32 [rows]).
+    """
+    import torch
+
+    if val.dim() != 2 or count.dim() != 1 or count.shape[0] != val.shape[0]:
+        raise ValueError("val must be [rows, k] and count [rows]")
+    for t in (val, count):
+        if not t.is_cuda or not t.is_contiguous():
+            raise TopkError(ERR_SHAPE, "nucleus inputs must be contiguous CUDA tensors")
+    rows, k = val.shape
+    if out is None:
+        out = (torch.empty((rows, k), dtype=torch.float32, device=val.device),
+               torch.empty((rows,), dtype=torch.int32, device=val.device))
+    if stream is None:
+        stream = torch.cuda.current_stream(val.device)
+    _check(tf_topk_nucleus_bf16(val.data_ptr(), count.data_ptr(), rows, k, float(temperature), float(top_p),
+                                out[0].data_ptr(), out[1].data_ptr(), stream.cuda_stream))
     return out
 
 
