@@ -551,9 +551,9 @@ __device__ __forceinline__ uint32_t prefilter_bound(uint32_t tmax, int nvalid, i
     return t0;
 }
 
-__device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, bool raw,
-                                             int nvalid, int32_t col_base, int k, SmemCore &sm, uint4 *stage,
-                                             int &run_i, int &chunk_i, int &free_i, int &run_len)
+__device__ __forceinline__ uint32_t select_candidates(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, bool raw,
+                                                      int nvalid, int k, SmemCore &sm, uint4 *stage, int run_i,
+                                                      int run_len)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -587,7 +587,6 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
     }
     __syncthreads();
     uint32_t n = sm.n_cand;
-    if (n == 0) return; // nothing reaches the threshold: the running list stands
     if (n > (uint32_t)kCandCap) {
         // heavy ties: stage every key in column order (below t_floor -> 0) and
         // select exactly
@@ -606,7 +605,16 @@ __device__ __forceinline__ void select_chunk(uint32_t (&kv)[kVecPerThread][4], u
         exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
         n = sm.n_cand; // == k
     }
+    return n;
+}
 
+// Second half of a chunk's selection, once its n > 0 candidates are in
+// sm.cand (the chunk's registers are no longer read): rank them, then merge
+// the chunk list into the running list (run_i, run_len).  Block-uniform.
+__device__ __forceinline__ void merge_candidates(uint32_t n, int32_t col_base, int k, SmemCore &sm, int &run_i,
+                                                 int &chunk_i, int &free_i, int &run_len)
+{
+    const int tid = threadIdx.x;
     // ---- rank the candidates: rank = number of larger composites
     if (tid < (int)n) {
         const uint32_t e = sm.cand[tid];
@@ -1261,6 +1269,43 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Loads the chunk of vectors [cbeg, min(v_end, cbeg + kChunkVecs)) of a row
+// into this thread's registers: vector i * kThreads + tid in kv[i]; vectors
+// past the chunk read as zero.  Inside the row's 16-byte-aligned body the
+// loads are plain; the row's ragged head and tail go through the edge path.
+__device__ __forceinline__ void load_chunk(uint32_t (&kv)[kVecPerThread][4], const uint4 *vbase,
+                                           const ChunkGeom &geo, int32_t cbeg, int32_t v_end, int32_t cols)
+{
+    const int tid = threadIdx.x;
+    const int32_t cend = min(v_end, cbeg + kChunkVecs);
+    const int nvalid = cend - cbeg;
+    if (nvalid == kChunkVecs && cbeg >= geo.vfull0 && cend <= geo.vfull1) {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const uint4 q = ld_stream(vbase + cbeg + i * kThreads + tid);
+            kv[i][0] = q.x;
+            kv[i][1] = q.y;
+            kv[i][2] = q.z;
+            kv[i][3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const int lv = i * kThreads + tid;
+            uint4 q = make_uint4(0, 0, 0, 0);
+            if (lv < nvalid) {
+                const int32_t v = cbeg + lv;
+                q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
+                                                       : load_edge_vector(geo.rowp, cols, geo.m, v);
+            }
+            kv[i][0] = q.x;
+            kv[i][1] = q.y;
+            kv[i][2] = q.z;
+            kv[i][3] = q.w;
+        }
+    }
+}
+
 // grid.x = rows * S; the launch groups each row's S CTAs into one cluster
 // (cluster rank == span).
 template <int S>
@@ -1293,48 +1338,30 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     __syncthreads();
     int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
 
+    uint32_t kv[kVecPerThread][4];
+    if (v_begin < v_end) load_chunk(kv, vbase, geo, v_begin, v_end, cols);
     for (int32_t cbeg = v_begin; cbeg < v_end; cbeg += kChunkVecs) {
-        geo.cbeg = cbeg;
-        geo.cend = min(v_end, cbeg + kChunkVecs);
-        const int nvalid = geo.cend - cbeg;
+        const int32_t cend = min(v_end, cbeg + kChunkVecs);
+        const int nvalid = cend - cbeg;
         const int32_t col_base = cbeg * 8 - geo.m;
-        const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && geo.cend <= geo.vfull1;
-        uint32_t kv[kVecPerThread][4];
-        if (full) {
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i) {
-                const uint4 q = ld_stream(vbase + cbeg + i * kThreads + tid);
-                kv[i][0] = q.x;
-                kv[i][1] = q.y;
-                kv[i][2] = q.z;
-                kv[i][3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i) {
-                const int lv = i * kThreads + tid;
-                uint4 q = make_uint4(0, 0, 0, 0);
-                if (lv < nvalid) {
-                    const int32_t v = cbeg + lv;
-                    q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
-                                                           : load_edge_vector(geo.rowp, cols, geo.m, v);
-                }
-                kv[i][0] = q.x;
-                kv[i][1] = q.y;
-                kv[i][2] = q.z;
-                kv[i][3] = q.w;
-            }
-        }
+        const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && cend <= geo.vfull1;
         // a full chunk inside the row: the max from the raw bits where it can be
         uint32_t tmax = 0;
         const bool raw = full && raw_tmax(kv, tmax);
-        if (!raw) tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+        if (!raw) {
+            geo.cbeg = cbeg;
+            geo.cend = cend;
+            tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+        }
         // The previous chunk's merge must be complete before its bound is read.
         // With two spans the barrier sits here, so the loads and keys above
         // overlap the slowest threads' merge; with more spans (shorter spans,
         // measured) it closes each chunk.
         if constexpr (S == 2) __syncthreads();
-        select_chunk(kv, tmax, raw, nvalid, col_base, k, sm, keys, run_i, chunk_i, free_i, run_len);
+        const uint32_t n = select_candidates(kv, tmax, raw, nvalid, k, sm, keys, run_i, run_len);
+        // the chunk's registers are free: the next chunk's loads fly during the merge
+        if (cend < v_end) load_chunk(kv, vbase, geo, cend, v_end, cols);
+        if (n) merge_candidates(n, col_base, k, sm, run_i, chunk_i, free_i, run_len);
         if constexpr (S != 2) __syncthreads();
     }
     __syncthreads(); // the last merge is complete
