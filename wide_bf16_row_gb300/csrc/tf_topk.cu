@@ -551,31 +551,75 @@ __device__ __forceinline__ uint32_t prefilter_bound(uint32_t tmax, int nvalid, i
     return t0;
 }
 
-__device__ __forceinline__ uint32_t select_candidates(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, bool raw,
-                                                      int nvalid, int k, SmemCore &sm, uint4 *stage, int run_i,
-                                                      int run_len)
+__device__ __forceinline__ uint32_t chunk_floor(uint32_t tmax, int nvalid, int k, SmemCore &sm, int run_i,
+                                                int run_len)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    uint32_t t_floor;
     if (run_len == k) {
         // steady state: a new entry must beat the running k-th strictly (every
         // column of this chunk is higher), and that bound needs no barrier
-        t_floor = (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
-    } else {
-        t_floor = max(key_floor(prefilter_bound(tmax, nvalid, k, sm)), 1u);
+        return (uint32_t)(sm.list[run_i][k - 1] >> 48) + 1u;
     }
+    return max(key_floor(prefilter_bound(tmax, nvalid, k, sm)), 1u);
+}
 
-    // ---- candidates: only threads whose max reaches t_floor hold any; each
-    //      such thread spills its keys, and its warp scans them one word per lane
+// Threads whose max reaches t_floor hold the chunk's candidates: each such
+// thread spills its keys into its own slots of `stage` (vector i at
+// stage[i * kThreads + tid]).  After this the chunk's registers are not read.
+__device__ __forceinline__ bool spill_hits(uint32_t (&kv)[kVecPerThread][4], uint32_t tmax, bool raw,
+                                           uint32_t t_floor, uint4 *stage)
+{
     const bool hit = tmax >= t_floor;
     if (hit) {
         if (raw) keys_in_place(kv);
-        raw = false;
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i)
-            stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+            stage[i * kThreads + threadIdx.x] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
     }
+    return hit;
+}
+
+// Heavy ties: every key of the chunk that reaches t_floor, in column order, in
+// `stage` (0 elsewhere), re-read from global memory (the registers that held
+// the chunk already carry the next one).  Keys are exact as in fix_keys:
+// columns outside the row and NaN become 0.
+__device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, ChunkGeom geo, int32_t cbeg,
+                                           int nvalid, int32_t col_base, uint32_t t_floor)
+{
+    const int tid = threadIdx.x;
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int lv = i * kThreads + tid;
+        uint32_t qw[4] = {0, 0, 0, 0};
+        if (lv < nvalid) {
+            const int32_t v = cbeg + lv;
+            const uint4 q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
+                                                               : load_edge_vector(geo.rowp, geo.cols, geo.m, v);
+            const uint32_t raw4[4] = {q.x, q.y, q.z, q.w};
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t key2 = keys_from_raw2(raw4[w]);
+                uint32_t out = 0;
+                for (int h = 0; h < 2; ++h) {
+                    const int32_t c = col_base + lv * 8 + 2 * w + h;
+                    uint32_t key = (key2 >> (16 * h)) & 0xFFFFu;
+                    if (c < 0 || c >= geo.cols || key > kKeyPosInf || key < kKeyNegInf || key < t_floor) key = 0;
+                    out |= key << (16 * h);
+                }
+                qw[w] = out;
+            }
+        }
+        stage[lv] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    }
+}
+
+// The chunk's candidates (keys >= t_floor) into sm.cand from the spilled
+// slots of the hit threads: each hit thread's warp scans its keys one word
+// per lane.  Returns their number n once every thread has pushed (a barrier);
+// above kCandCap (heavy ties) the chunk is restaged and selected exactly, and
+// n = k.  Block-uniform.
+__device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, int k, SmemCore &sm, uint4 *stage,
+                                                    const uint4 *vbase, const ChunkGeom &geo, int32_t cbeg,
+                                                    int nvalid, int32_t col_base)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncwarp();
     for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits; hits &= hits - 1) {
         const int src = warp * 32 + __ffs(hits) - 1;
@@ -588,19 +632,7 @@ __device__ __forceinline__ uint32_t select_candidates(uint32_t (&kv)[kVecPerThre
     __syncthreads();
     uint32_t n = sm.n_cand;
     if (n > (uint32_t)kCandCap) {
-        // heavy ties: stage every key in column order (below t_floor -> 0) and
-        // select exactly
-        if (raw) keys_in_place(kv);
-#pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            uint32_t q[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t lo = kv[i][w] & 0xFFFFu, hi = kv[i][w] >> 16;
-                q[w] = (lo >= t_floor ? lo : 0u) | ((hi >= t_floor ? hi : 0u) << 16);
-            }
-            stage[i * kThreads + tid] = make_uint4(q[0], q[1], q[2], q[3]);
-        }
+        restage_chunk(stage, vbase, geo, cbeg, nvalid, col_base, t_floor);
         __syncthreads();
         exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
         n = sm.n_cand; // == k
@@ -1353,18 +1385,17 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
             geo.cend = cend;
             tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
         }
-        // The previous chunk's merge must be complete before its bound is read.
-        // With two spans the barrier sits here, so the loads and keys above
-        // overlap the slowest threads' merge; with more spans (shorter spans,
-        // measured) it closes each chunk.
-        if constexpr (S == 2) __syncthreads();
-        const uint32_t n = select_candidates(kv, tmax, raw, nvalid, k, sm, keys, run_i, run_len);
-        // the chunk's registers are free: the next chunk's loads fly during the merge
-        if (cend < v_end) load_chunk(kv, vbase, geo, cend, v_end, cols);
+        const uint32_t t_floor = chunk_floor(tmax, nvalid, k, sm, run_i, run_len);
+        const bool hit = spill_hits(kv, tmax, raw, t_floor, keys);
+        // the chunk's registers are free: the next chunk's loads fly during
+        // the candidate scan, the rank and the merge
+        const bool more = cend < v_end;
+        if (more) load_chunk(kv, vbase, geo, cend, v_end, cols);
+        const uint32_t n = push_candidates(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base);
+        if (n > (uint32_t)kCandCap && more) load_chunk(kv, vbase, geo, cend, v_end, cols); // reissued after the exact path
         if (n) merge_candidates(n, col_base, k, sm, run_i, chunk_i, free_i, run_len);
-        if constexpr (S != 2) __syncthreads();
+        __syncthreads(); // the merge is complete before the next chunk reads its bound
     }
-    __syncthreads(); // the last merge is complete
 
     // ---- push this span's list into the leader's shared memory
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); // every CTA has started
