@@ -234,24 +234,6 @@ __device__ __forceinline__ int count_greater(const uint64_t *list, int len, uint
     return lo;
 }
 
-// out = top-k of the union of two disjoint descending lists (rank by merge).
-__device__ __forceinline__ void merge_lists(const uint64_t *a, int la, const uint64_t *b, int lb,
-                                            uint64_t *out, int k)
-{
-    for (int t = threadIdx.x; t < la + lb; t += kThreads) {
-        uint64_t x;
-        int pos;
-        if (t < la) {
-            x = a[t];
-            pos = t + count_greater(b, lb, x);
-        } else {
-            x = b[t - la];
-            pos = (t - la) + count_greater(a, la, x);
-        }
-        if (pos < k) out[pos] = x;
-    }
-}
-
 __device__ __forceinline__ uint32_t block_sum(uint32_t v, SmemCore &sm, int parity)
 {
     v = __reduce_add_sync(0xFFFFFFFFu, v);
@@ -263,9 +245,11 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, SmemCore &sm, int pari
     return s;
 }
 
-__device__ __forceinline__ void push_candidate(SmemCore &sm, uint32_t key, int local)
+// The candidate counter only grows within a chunk loop: a chunk's slots count
+// from `base`, the counter's value when the chunk began.
+__device__ __forceinline__ void push_candidate(SmemCore &sm, uint32_t key, int local, uint32_t base)
 {
-    const uint32_t slot = atomicAdd(&sm.n_cand, 1u);
+    const uint32_t slot = atomicAdd(&sm.n_cand, 1u) - base;
     if (slot < (uint32_t)kCandCap) {
         sm.cand[slot] = (canon(key) << 16) | (0xFFFFu - (uint32_t)local);
         sm.cand_raw[slot] = (uint16_t)raw_from_key(key);
@@ -349,9 +333,9 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
             if (key == 0) continue;
             const uint32_t c = canon(key);
             if (c > kstar) {
-                push_candidate(sm, key, 2 * w + h);
+                push_candidate(sm, key, 2 * w + h, 0u);
             } else if (c == kstar) {
-                if (ord < need) push_candidate(sm, key, 2 * w + h);
+                if (ord < need) push_candidate(sm, key, 2 * w + h, 0u);
                 ++ord;
             }
         }
@@ -614,10 +598,11 @@ __device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, Chu
 // slots of the hit threads: each hit thread's warp scans its keys one word
 // per lane.  Returns their number n once every thread has pushed (a barrier);
 // above kCandCap (heavy ties) the chunk is restaged and selected exactly, and
-// n = k.  Block-uniform.
+// n = k.  `base` (block-uniform) is the candidate counter's value before the
+// chunk and after it.  Block-uniform.
 __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, int k, SmemCore &sm, uint4 *stage,
                                                     const uint4 *vbase, const ChunkGeom &geo, int32_t cbeg,
-                                                    int nvalid, int32_t col_base)
+                                                    int nvalid, int32_t col_base, uint32_t &base)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncwarp();
@@ -626,29 +611,39 @@ __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, 
         const int lv = (lane >> 2) * kThreads + src;
         const uint32_t key2 = reinterpret_cast<const uint32_t *>(stage)[lv * 4 + (lane & 3)];
         const int local = lv * 8 + 2 * (lane & 3);
-        if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local);
-        if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1);
+        if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local, base);
+        if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1, base);
     }
     __syncthreads();
-    uint32_t n = sm.n_cand;
+    const uint32_t total = sm.n_cand;
+    uint32_t n = total - base;
+    base = total;
     if (n > (uint32_t)kCandCap) {
         restage_chunk(stage, vbase, geo, cbeg, nvalid, col_base, t_floor);
         __syncthreads();
-        exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm);
+        exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm); // counts from 0
         n = sm.n_cand; // == k
+        base = n;
     }
     return n;
 }
 
 // Second half of a chunk's selection, once its n > 0 candidates are in
-// sm.cand (the chunk's registers are no longer read): rank them, then merge
-// the chunk list into the running list (run_i, run_len).  Block-uniform.
+// sm.cand (the chunk's registers are no longer read): every candidate and
+// every running entry finds its place in the merged list at once.  A
+// candidate's place is its rank among the candidates plus the running entries
+// above it; a running entry's is its index plus the candidates above it.  The
+// merged list goes to list[free_i], which becomes the running list.  No
+// barrier: the caller's next one orders this before the list is read.
 __device__ __forceinline__ void merge_candidates(uint32_t n, int32_t col_base, int k, SmemCore &sm, int &run_i,
-                                                 int &chunk_i, int &free_i, int &run_len)
+                                                 int &free_i, int &run_len)
 {
     const int tid = threadIdx.x;
-    // ---- rank the candidates: rank = number of larger composites
+    const uint64_t *run = sm.list[run_i];
+    uint64_t *out = sm.list[free_i];
+    const int rl = run_len;
     if (tid < (int)n) {
+        // rank = number of larger composites
         const uint32_t e = sm.cand[tid];
         uint32_t rank = 0;
         const uint4 *c4 = reinterpret_cast<const uint4 *>(sm.cand);
@@ -658,23 +653,28 @@ __device__ __forceinline__ void merge_candidates(uint32_t n, int32_t col_base, i
             rank += (q.x > e) + (q.y > e) + (q.z > e) + (q.w > e);
         }
         for (uint32_t u = nq * 4; u < n; ++u) rank += sm.cand[u] > e;
-        if (rank < (uint32_t)k) sm.list[chunk_i][rank] = entry_from_cand(e, sm.cand_raw[tid], col_base);
+        if (rank < (uint32_t)k) {
+            const uint64_t x = entry_from_cand(e, sm.cand_raw[tid], col_base);
+            const int pos = (int)rank + count_greater(run, rl, x);
+            if (pos < k) out[pos] = x;
+        }
     }
-    __syncthreads();
-    if (tid == 0) sm.n_cand = 0; // every thread has read n; the next chunk pushes from 0
-    const int chunk_len = min((int)n, k);
-    if (run_len == 0) {
-        const int t = run_i;
-        run_i = chunk_i;
-        chunk_i = t;
-    } else if (chunk_len > 0) {
-        merge_lists(sm.list[run_i], run_len, sm.list[chunk_i], chunk_len, sm.list[free_i], k);
-        const int t = run_i;
-        run_i = free_i;
-        free_i = t;
+    const int j = kThreads - 1 - tid; // running entries on the highest threads
+    if (j < rl) {
+        const uint64_t x = run[j];
+        const uint64_t xs = x >> 16; // (key, ~column): the original bits never decide
+        int above = 0;
+        for (uint32_t u = 0; u < n; ++u) {
+            const uint32_t c = sm.cand[u];
+            const uint32_t col = (uint32_t)(col_base + (int32_t)(0xFFFFu - (c & 0xFFFFu)));
+            above += ((((uint64_t)(c >> 16)) << 32) | (uint64_t)(~col)) > xs;
+        }
+        if (j + above < k) out[j + above] = x;
     }
-    run_len = min(k, run_len + chunk_len);
-    // the next reader of the running list is behind a barrier of the caller
+    const int t = run_i;
+    run_i = free_i;
+    free_i = t;
+    run_len = min(k, rl + (int)min(n, (uint32_t)k));
 }
 
 
@@ -1368,7 +1368,8 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         sm.n_cand = 0;
     }
     __syncthreads();
-    int run_i = 0, chunk_i = 1, free_i = 2, run_len = 0;
+    int run_i = 0, free_i = 1, run_len = 0;
+    uint32_t cand_base = 0; // the candidate counter before this chunk (block-uniform)
 
     uint32_t kv[kVecPerThread][4];
     if (v_begin < v_end) load_chunk(kv, vbase, geo, v_begin, v_end, cols);
@@ -1391,9 +1392,9 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         // the candidate scan, the rank and the merge
         const bool more = cend < v_end;
         if (more) load_chunk(kv, vbase, geo, cend, v_end, cols);
-        const uint32_t n = push_candidates(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base);
+        const uint32_t n = push_candidates(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base, cand_base);
         if (n > (uint32_t)kCandCap && more) load_chunk(kv, vbase, geo, cend, v_end, cols); // reissued after the exact path
-        if (n) merge_candidates(n, col_base, k, sm, run_i, chunk_i, free_i, run_len);
+        if (n) merge_candidates(n, col_base, k, sm, run_i, free_i, run_len);
         __syncthreads(); // the merge is complete before the next chunk reads its bound
     }
 
