@@ -43,39 +43,44 @@ def build(mutant: int = 0, force: bool = False) -> Path:
     return out
 
 
+DTYPES = {"bf16": (0, np.uint16), "f16": (1, np.uint16), "f32": (2, np.uint32)}
+
+
 class Oracle:
     """ctypes handle on one build of the oracle library."""
 
     def __init__(self, mutant: int = 0):
         self.mutant = mutant
         self._lib = ctypes.CDLL(str(build(mutant)))
-        fn = self._lib.oracle_topk_bf16
+        fn = self._lib.oracle_topk
         fn.restype = ctypes.c_int
-        fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                        ctypes.c_void_p, ctypes.c_int32]
         self._fn = fn
 
-    def topk(self, logits: np.ndarray, cols: int, k: int, nthreads: int | None = None):
-        """Top-k of every row of ``logits`` (uint16 bf16 bits, shape rows x row_stride).
+    def topk(self, logits: np.ndarray, cols: int, k: int, nthreads: int | None = None, dtype: str = "bf16"):
+        """Top-k of every row of ``logits`` (bit patterns of ``dtype``: uint16 for
+        "bf16" and "f16", uint32 for "f32"; shape rows x row_stride).
 
-        Returns ``(idx int32[rows,k], val uint16[rows,k], count int32[rows],
+        Returns ``(idx int32[rows,k], val [rows,k] bits of dtype, count int32[rows],
         mask uint32[rows])``.
         """
-        x = np.ascontiguousarray(logits, dtype=np.uint16)
+        code, bits = DTYPES[dtype]
+        x = np.ascontiguousarray(logits, dtype=bits)
         if x.ndim != 2:
             raise ValueError("logits must be 2-D (rows x row_stride)")
         rows, stride = x.shape
         idx = np.empty((rows, k), np.int32)
-        val = np.empty((rows, k), np.uint16)
+        val = np.empty((rows, k), bits)
         count = np.empty(rows, np.int32)
         mask = np.empty(rows, np.uint32)
         if nthreads is None:
             nthreads = host_cores()
-        rc = self._fn(x.ctypes.data, rows, cols, stride, k, idx.ctypes.data, val.ctypes.data,
+        rc = self._fn(x.ctypes.data, code, rows, cols, stride, k, idx.ctypes.data, val.ctypes.data,
                       count.ctypes.data, mask.ctypes.data, int(nthreads))
         if rc != 0:
-            raise RuntimeError(f"oracle_topk_bf16 failed with status {rc}")
+            raise RuntimeError(f"oracle_topk failed with status {rc}")
         return idx, val, count, mask
 
 
@@ -90,9 +95,9 @@ def host_cores() -> int:
 _default: Oracle | None = None
 
 
-def topk(logits: np.ndarray, cols: int, k: int, nthreads: int | None = None):
+def topk(logits: np.ndarray, cols: int, k: int, nthreads: int | None = None, dtype: str = "bf16"):
     """Module-level shortcut on the (unmutated) oracle."""
     global _default
     if _default is None:
         _default = Oracle(0)
-    return _default.topk(logits, cols, k, nthreads)
+    return _default.topk(logits, cols, k, nthreads, dtype)

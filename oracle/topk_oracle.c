@@ -26,6 +26,10 @@
  *     taken over columns [0, cols) only (padding is never looked at);
  *   - slots count..k-1 hold index -1 and value bits 0x7FC0.
  *
+ * The same definition is applied to fp16 and fp32 logits (the pages' method
+ * is stated for bf16; the other two formats keep every convention above, and
+ * their empty slots hold the format's quiet NaN, 0x7E00 and 0x7FC00000).
+ *
  * Method: the plain definition.  Every value is widened to double (exact for
  * bf16), the non-NaN columns are stable-sorted by value descending with a
  * merge sort, and the first min(k, n) are reported.  Parity is pinned by the
@@ -46,6 +50,8 @@
 #define ORACLE_MUTANT 0
 #endif
 
+enum { ORACLE_BF16 = 0, ORACLE_F16 = 1, ORACLE_F32 = 2 };
+
 /* A bf16 value is the top half of an IEEE binary32; widening it to double is
  * exact. */
 static double bf16_bits_to_double(uint16_t bits)
@@ -54,6 +60,70 @@ static double bf16_bits_to_double(uint16_t bits)
     float f;
     memcpy(&f, &word, sizeof f);
     return (double)f;
+}
+
+/* IEEE binary16: sign, 5 exponent bits (bias 15), 10 fraction bits.  Every
+ * value is an integer times a power of two, so ldexp gives it exactly. */
+static double f16_bits_to_double(uint16_t bits)
+{
+    const int sign = bits >> 15, e = (bits >> 10) & 0x1F, m = bits & 0x3FF;
+    double v;
+    if (e == 0x1F)
+        v = m ? NAN : INFINITY;
+#if ORACLE_MUTANT == 10 /* mutant: subnormals read as if normal */
+    else
+        v = ldexp(1024.0 + m, e - 25);
+#else
+    else if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else
+        v = ldexp(1024.0 + m, e - 25);
+#endif
+    return sign ? -v : v;
+}
+
+static double f32_bits_to_double(uint32_t bits)
+{
+#if ORACLE_MUTANT == 11 /* mutant: only the high half of an fp32 is read */
+    bits &= 0xFFFF0000u;
+#endif
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static size_t elem_size(int32_t dtype) { return dtype == ORACLE_F32 ? 4 : 2; }
+
+static double elem_value(const void *row, int32_t dtype, int64_t c)
+{
+    if (dtype == ORACLE_F32) return f32_bits_to_double(((const uint32_t *)row)[c]);
+    if (dtype == ORACLE_F16) return f16_bits_to_double(((const uint16_t *)row)[c]);
+    return bf16_bits_to_double(((const uint16_t *)row)[c]);
+}
+
+/* out[i] = the original bits of row[c] */
+static void elem_copy(void *out, int64_t i, const void *row, int64_t c, int32_t dtype)
+{
+    if (dtype == ORACLE_F32)
+        ((uint32_t *)out)[i] = ((const uint32_t *)row)[c];
+    else
+        ((uint16_t *)out)[i] = ((const uint16_t *)row)[c];
+}
+
+/* out[i] = the empty-slot value: the format's quiet NaN */
+static void elem_empty(void *out, int64_t i, int32_t dtype)
+{
+#if ORACLE_MUTANT == 8 /* mutant: empty slots keep value bits 0 */
+    if (dtype == ORACLE_F32)
+        ((uint32_t *)out)[i] = 0;
+    else
+        ((uint16_t *)out)[i] = 0;
+#else
+    if (dtype == ORACLE_F32)
+        ((uint32_t *)out)[i] = 0x7FC00000u;
+    else
+        ((uint16_t *)out)[i] = dtype == ORACLE_F16 ? 0x7E00 : 0x7FC0;
+#endif
 }
 
 /* Does a go before b in "score descending" order?  Equal scores return 0, so
@@ -100,9 +170,8 @@ struct row_scratch {
 };
 
 /* One row: x[0..cols) -> k output slots, a count and a mask. */
-static void oracle_row(const uint16_t *x, int64_t cols, int32_t k, int32_t *out_idx,
-                       uint16_t *out_val, int32_t *out_count, uint32_t *out_mask,
-                       struct row_scratch *s)
+static void oracle_row(const void *x, int32_t dtype, int64_t cols, int32_t k, int32_t *out_idx,
+                       void *out_val, int32_t *out_count, uint32_t *out_mask, struct row_scratch *s)
 {
     uint32_t mask = 0;
     int64_t n = 0;
@@ -112,7 +181,7 @@ static void oracle_row(const uint16_t *x, int64_t cols, int32_t k, int32_t *out_
     int64_t scan = cols;
 #endif
     for (int64_t c = 0; c < scan; ++c) {
-        double v = bf16_bits_to_double(x[c]);
+        double v = elem_value(x, dtype, c);
 #if ORACLE_MUTANT == 4 /* mutant: -0 ranks below +0 */
         if (v == 0.0 && signbit(v)) v = -1e-300;
 #endif
@@ -137,15 +206,11 @@ static void oracle_row(const uint16_t *x, int64_t cols, int32_t k, int32_t *out_
     int64_t m = n < (int64_t)k ? n : (int64_t)k;
     for (int64_t i = 0; i < m; ++i) {
         out_idx[i] = (int32_t)s->idx[i];
-        out_val[i] = x[s->idx[i]];
+        elem_copy(out_val, i, x, s->idx[i], dtype);
     }
     for (int64_t i = m; i < k; ++i) {
         out_idx[i] = -1;
-#if ORACLE_MUTANT == 8 /* mutant: empty slots keep value bits 0 */
-        out_val[i] = 0;
-#else
-        out_val[i] = 0x7FC0;
-#endif
+        elem_empty(out_val, i, dtype);
     }
 #if ORACLE_MUTANT == 7 /* mutant: the count ignores NaN columns */
     *out_count = (int32_t)((int64_t)k < cols ? k : cols);
@@ -156,11 +221,12 @@ static void oracle_row(const uint16_t *x, int64_t cols, int32_t k, int32_t *out_
 }
 
 struct job {
-    const uint16_t *logits;
+    const unsigned char *logits;
+    int32_t dtype;
     int64_t row_begin, row_end, cols, row_stride;
     int32_t k;
     int32_t *out_idx;
-    uint16_t *out_val;
+    unsigned char *out_val;
     int32_t *out_count;
     uint32_t *out_mask;
     int status;
@@ -177,14 +243,15 @@ static void *run_job(void *arg)
     if (!s.idx || !s.tmp || !s.score) {
         j->status = -2;
     } else {
+        const size_t es = elem_size(j->dtype);
         for (int64_t r = j->row_begin; r < j->row_end; ++r) {
 #if ORACLE_MUTANT == 9 /* mutant: rows are read as if packed (stride ignored) */
-            const uint16_t *row = j->logits + r * j->cols;
+            const unsigned char *row = j->logits + (size_t)(r * j->cols) * es;
 #else
-            const uint16_t *row = j->logits + r * j->row_stride;
+            const unsigned char *row = j->logits + (size_t)(r * j->row_stride) * es;
 #endif
-            oracle_row(row, j->cols, j->k, j->out_idx + r * j->k, j->out_val + r * j->k,
-                       j->out_count + r, j->out_mask + r, &s);
+            oracle_row(row, j->dtype, j->cols, j->k, j->out_idx + r * j->k,
+                       j->out_val + (size_t)(r * j->k) * es, j->out_count + r, j->out_mask + r, &s);
         }
         j->status = 0;
     }
@@ -195,21 +262,22 @@ static void *run_job(void *arg)
 }
 
 /*
- * Exact top-k of every row of a bf16 matrix, on the host.
- *   logits      host array of bf16 bit patterns, rows x row_stride elements;
- *               columns [cols, row_stride) are padding and are never read.
+ * Exact top-k of every row of a bf16, fp16 or fp32 matrix, on the host.
+ *   logits      host array of bit patterns, rows x row_stride elements of
+ *               dtype (0 bf16, 1 fp16, 2 fp32); columns [cols, row_stride)
+ *               are padding and are never read.
  *   k           any k >= 1 (the oracle itself has no upper limit).
- *   out_idx     rows x k int32, out_val rows x k bf16 bits,
+ *   out_idx     rows x k int32, out_val rows x k elements of dtype (bits),
  *   out_count   rows int32, out_mask rows uint32.
  *   nthreads    worker threads (rows are split into contiguous ranges); < 1
  *               means one.
  * Returns 0, -1 for bad arguments, -2 when scratch memory cannot be had.
  */
-int oracle_topk_bf16(const uint16_t *logits, int64_t rows, int64_t cols, int64_t row_stride,
-                     int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
-                     uint32_t *out_mask, int32_t nthreads)
+int oracle_topk(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_mask, int32_t nthreads)
 {
     if (rows < 0 || cols < 1 || row_stride < cols || k < 1) return -1;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_F16 && dtype != ORACLE_F32) return -1;
     if (rows == 0) return 0;
     if (!logits || !out_idx || !out_val || !out_count || !out_mask) return -1;
     if (nthreads < 1) nthreads = 1;
@@ -225,8 +293,8 @@ int oracle_topk_bf16(const uint16_t *logits, int64_t rows, int64_t cols, int64_t
     int64_t per = rows / nthreads, extra = rows % nthreads, r0 = 0;
     for (int32_t t = 0; t < nthreads; ++t) {
         int64_t cnt = per + (t < extra ? 1 : 0);
-        jobs[t] = (struct job){logits, r0, r0 + cnt, cols, row_stride, k,
-                               out_idx, out_val, out_count, out_mask, -3};
+        jobs[t] = (struct job){(const unsigned char *)logits, dtype, r0, r0 + cnt, cols, row_stride, k,
+                               out_idx, (unsigned char *)out_val, out_count, out_mask, -3};
         r0 += cnt;
     }
     int started = 0;
@@ -245,4 +313,13 @@ int oracle_topk_bf16(const uint16_t *logits, int64_t rows, int64_t cols, int64_t
     free(jobs);
     free(tids);
     return status;
+}
+
+/* The bf16 entry: oracle_topk with dtype 0. */
+int oracle_topk_bf16(const uint16_t *logits, int64_t rows, int64_t cols, int64_t row_stride,
+                     int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
+                     uint32_t *out_mask, int32_t nthreads)
+{
+    return oracle_topk(logits, ORACLE_BF16, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
+                       nthreads);
 }

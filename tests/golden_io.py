@@ -18,6 +18,8 @@ def load(path: Path) -> dict:
         key, *rest = line.split()
         if key in ("cols", "stride", "k"):
             meta[key] = int(rest[0])
+        elif key == "dtype":
+            meta[key] = rest[0]
         elif key == "row":
             rows.append([int(t, 16) for t in rest])
         elif key == "idx":
@@ -30,14 +32,17 @@ def load(path: Path) -> dict:
             mask.append(int(rest[0]))
         else:
             raise ValueError(f"{path.name}: unknown key {key}")
+    dtype = meta.get("dtype", "bf16")
+    bits = np.uint32 if dtype == "f32" else np.uint16
     return {
         "name": path.stem,
+        "dtype": dtype,
         "cols": meta["cols"],
         "stride": meta["stride"],
         "k": meta["k"],
-        "logits": np.array(rows, np.uint16),
+        "logits": np.array(rows, bits),
         "idx": np.array(idx, np.int32),
-        "val": np.array(val, np.uint16),
+        "val": np.array(val, bits),
         "count": np.array(count, np.int32),
         "mask": np.array(mask, np.uint32),
     }

@@ -66,13 +66,13 @@ def brute_force_row(bits, k):
     return idx, val, len(picked), mask
 
 
-def check_against(oracle: Oracle, logits: np.ndarray, cols: int, k: int, expect) -> None:
-    idx, val, count, mask = oracle.topk(logits, cols, k, nthreads=2)
+def check_against(oracle: Oracle, logits: np.ndarray, cols: int, k: int, expect, dtype: str = "bf16") -> None:
+    idx, val, count, mask = oracle.topk(logits, cols, k, nthreads=2, dtype=dtype)
     e_idx, e_val, e_count, e_mask = expect
     np.testing.assert_array_equal(count, np.asarray(e_count, np.int32))
     np.testing.assert_array_equal(mask, np.asarray(e_mask, np.uint32))
     np.testing.assert_array_equal(idx, np.asarray(e_idx, np.int32))
-    np.testing.assert_array_equal(val, np.asarray(e_val, np.uint16))
+    np.testing.assert_array_equal(val, np.asarray(e_val, np.uint32 if dtype == "f32" else np.uint16))
 
 
 # --------------------------------------------------------------------------- pins
@@ -176,12 +176,12 @@ def pin_edge_rows(oracle: Oracle) -> None:
 
 
 def pin_golden(oracle: Oracle) -> None:
-    """Hand-derived fixtures under tests/golden/."""
+    """Hand-derived fixtures under tests/golden/ (bf16, fp16 and fp32)."""
     fixtures = golden_io.all_fixtures()
-    assert len(fixtures) >= 5
+    assert len(fixtures) >= 5 and {fx["dtype"] for fx in fixtures} == {"bf16", "f16", "f32"}
     for fx in fixtures:
         check_against(oracle, fx["logits"], fx["cols"], fx["k"],
-                      (fx["idx"], fx["val"], fx["count"], fx["mask"]))
+                      (fx["idx"], fx["val"], fx["count"], fx["mask"]), dtype=fx["dtype"])
 
 
 def pin_invariants(oracle: Oracle) -> None:
@@ -211,8 +211,90 @@ def pin_invariants(oracle: Oracle) -> None:
                 assert v < vals[-1] or (v == vals[-1] and c > sel[-1])
 
 
+# ---- fp16 and fp32: the same definition, values decoded by numpy's own types
+
+EMPTY_BY_DTYPE = {"f16": 0x7E00, "f32": 0x7FC00000}
+
+
+def numpy_values(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Bit patterns -> float64 through numpy's float16 / float32 (not the oracle's decode)."""
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns widen to NaN
+        if dtype == "f16":
+            return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+        return np.asarray(bits, np.uint32).view(np.float32).astype(np.float64)
+
+
+def reference_rows(x: np.ndarray, cols: int, k: int, dtype: str):
+    """Per row: non-NaN columns in stable order of -value, truncated to k; mask
+    and empty slots by the readings."""
+    rows = x.shape[0]
+    bits = np.uint32 if dtype == "f32" else np.uint16
+    e_idx = np.full((rows, k), EMPTY_IDX, np.int32)
+    e_val = np.full((rows, k), EMPTY_BY_DTYPE[dtype], bits)
+    e_count = np.zeros(rows, np.int32)
+    e_mask = np.zeros(rows, np.uint32)
+    for r in range(rows):
+        v = numpy_values(x[r, :cols], dtype)
+        order = [c for c in np.argsort(-v, kind="stable") if not math.isnan(v[c])]
+        n = min(k, len(order))
+        e_idx[r, :n] = order[:n]
+        e_val[r, :n] = x[r, order[:n]]
+        e_count[r] = n
+        e_mask[r] = (1 if np.isnan(v).any() else 0) | (2 if (v == np.inf).any() else 0) \
+            | (4 if (v == -np.inf).any() else 0)
+    return e_idx, e_val, e_count, e_mask
+
+
+def brute_force_rows(x: np.ndarray, k: int, dtype: str):
+    """Repeated argmax over numpy-decoded values (strict > keeps the lowest column)."""
+    rows, cols = x.shape
+    bits = np.uint32 if dtype == "f32" else np.uint16
+    e_idx = np.full((rows, k), EMPTY_IDX, np.int32)
+    e_val = np.full((rows, k), EMPTY_BY_DTYPE[dtype], bits)
+    e_count = np.zeros(rows, np.int32)
+    e_mask = np.zeros(rows, np.uint32)
+    for r in range(rows):
+        vals = [float(v) for v in numpy_values(x[r], dtype)]
+        used, picked = set(), []
+        for _ in range(k):
+            best = None
+            for c, v in enumerate(vals):
+                if c not in used and not math.isnan(v) and (best is None or v > vals[best]):
+                    best = c
+            if best is None:
+                break
+            used.add(best)
+            picked.append(best)
+        e_idx[r, :len(picked)] = picked
+        e_val[r, :len(picked)] = x[r, picked]
+        e_count[r] = len(picked)
+        e_mask[r] = sum(b for b, hit in ((1, any(math.isnan(v) for v in vals)), (2, math.inf in vals),
+                                          (4, -math.inf in vals)) if hit)
+    return e_idx, e_val, e_count, e_mask
+
+
+def pin_f16_f32_alphabet(oracle: Oracle) -> None:
+    """Every row of length 1..3 over each format's special alphabet, k = 1..4,
+    against the repeated-argmax brute force."""
+    for dtype, alpha in (("f16", synth.special_alphabet_f16()), ("f32", synth.special_alphabet_f32())):
+        for length in (1, 2, 3):
+            rows = np.array(list(itertools.product(alpha, repeat=length)), alpha.dtype)
+            for k in (1, 2, 4):
+                check_against(oracle, rows, length, k, brute_force_rows(rows, k, dtype), dtype=dtype)
+
+
+def pin_f16_f32_argsort(oracle: Oracle) -> None:
+    """Random mixed rows (subnormals, specials, copies, low-half near-ties,
+    padded strides) against numpy's stable argsort of -value."""
+    for dtype, gen in (("f16", synth.mixed_rows_f16), ("f32", synth.mixed_rows_f32)):
+        for seed, cols, stride, k in ((1, 1000, 1000, 64), (2, 4099, 4160, 20), (3, 257, 260, 1),
+                                      (4, 300, 300, 300)):
+            x = gen(4, cols, seed=seed, row_stride=stride, special_frac=0.08, dup_frac=0.05)
+            check_against(oracle, x, cols, k, reference_rows(x, cols, k, dtype), dtype=dtype)
+
+
 PINS = [pin_bruteforce_alphabet, pin_bruteforce_random, pin_numpy_argsort, pin_full_sort,
-        pin_prefix, pin_edge_rows, pin_golden, pin_invariants]
+        pin_prefix, pin_edge_rows, pin_golden, pin_invariants, pin_f16_f32_alphabet, pin_f16_f32_argsort]
 
 
 @pytest.fixture(scope="module")
@@ -235,6 +317,8 @@ MUTANTS = {
     7: "count ignores NaN columns",
     8: "empty slots hold value bits 0",
     9: "row stride ignored",
+    10: "fp16 subnormals read as normals",
+    11: "fp32 read from its high half only",
 }
 
 

@@ -205,6 +205,68 @@ def mixed_rows(rows: int, cols: int, seed: int, row_stride: int | None = None,
     return _pad(rng, vals, stride)
 
 
+
+# ---------------------------------------------------------------- fp16 and fp32 rows
+
+def special_alphabet_f16() -> np.ndarray:
+    """fp16 patterns for -inf, -max, -1, -min subnormal, -0, +0, +min subnormal,
+    +1, +max, +inf and two NaNs (quiet positive, signalling-style negative)."""
+    return np.array([0xFC00, 0xFBFF, 0xBC00, 0x8001, 0x8000, 0x0000, 0x0001, 0x3C00, 0x7BFF, 0x7C00,
+                     0x7E00, 0xFC01], dtype=np.uint16)
+
+
+def special_alphabet_f32() -> np.ndarray:
+    """fp32 patterns for -inf, -max, -1, -min subnormal, -0, +0, +min subnormal,
+    1, the next float above 1 (differs only in the low half), +max, +inf and
+    two NaNs."""
+    return np.array([0xFF800000, 0xFF7FFFFF, 0xBF800000, 0x80000001, 0x80000000, 0x00000000, 0x00000001,
+                     0x3F800000, 0x3F800001, 0x7F7FFFFF, 0x7F800000, 0x7FC00000, 0xFF800001],
+                    dtype=np.uint32)
+
+
+def mixed_rows_f16(rows: int, cols: int, seed: int, row_stride: int | None = None,
+                   special_frac: float = 0.05, dup_frac: float = 0.02, sigma: float = 2.0) -> np.ndarray:
+    """fp16 bit patterns (uint16): normal rows rounded to fp16, sprinkled with
+    the fp16 specials, copies and random subnormals; padding is random bits."""
+    rng = np.random.default_rng(seed)
+    vals = (rng.standard_normal((rows, cols)) * sigma).astype(np.float16).view(np.uint16)
+    _duplicate(rng, vals, dup_frac)
+    n = int(cols * special_frac)
+    if n:
+        alpha = special_alphabet_f16()
+        for r in range(rows):
+            pos = rng.choice(cols, size=n, replace=False)
+            pick = alpha[rng.integers(0, len(alpha), size=n)]
+            sub = rng.integers(1, 0x400, size=n, dtype=np.uint16) | (rng.integers(0, 2, size=n, dtype=np.uint16) << np.uint16(15))
+            vals[r, pos] = np.where(rng.random(n) < 0.3, sub, pick)
+    stride = cols if row_stride is None else row_stride
+    return _pad(rng, vals, stride)
+
+
+def mixed_rows_f32(rows: int, cols: int, seed: int, row_stride: int | None = None,
+                   special_frac: float = 0.05, dup_frac: float = 0.02, sigma: float = 2.0) -> np.ndarray:
+    """fp32 bit patterns (uint32): normal rows, sprinkled with the fp32
+    specials, copies, near-ties that differ only in the low 16 bits, and
+    subnormals; padding is random bits."""
+    rng = np.random.default_rng(seed)
+    vals = (rng.standard_normal((rows, cols)) * sigma).astype(np.float32).view(np.uint32)
+    _duplicate(rng, vals, dup_frac)
+    n = int(cols * special_frac)
+    if n:
+        alpha = special_alphabet_f32()
+        for r in range(rows):
+            pos = rng.choice(cols, size=n, replace=False)
+            pick = alpha[rng.integers(0, len(alpha), size=n)]
+            near = (vals[r, rng.integers(0, cols, size=n)] ^ rng.integers(1, 1 << 16, size=n, dtype=np.uint32))
+            vals[r, pos] = np.where(rng.random(n) < 0.4, near, pick)
+    stride = cols if row_stride is None else row_stride
+    if stride == cols:
+        return np.ascontiguousarray(vals)
+    out = rng.integers(0, 1 << 32, size=(rows, stride), dtype=np.uint32)
+    out[:, :cols] = vals
+    return out
+
+
 def ranked_lists(rows: int, k: int, seed: int) -> tuple[np.ndarray, np.ndarray]:
     """Lists shaped like a top-k's output, for the step that consumes them:
     ``(val uint16 [rows, k], count int32 [rows])``, each row's first ``count``
