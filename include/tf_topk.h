@@ -250,6 +250,49 @@ int tf_topk_bf16_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t
 int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature,
                          float top_p, float *out_prob, int32_t *out_keep, void *stream);
 
+/*
+ * Top-k of bf16, fp16 or fp32 rows, k up to TF_TOPK_MAX_K_WIDE.
+ *
+ * The operation of tf_topk_bf16 (TensorFold PR #713, change 3: score
+ * descending, the lower column first; the "Exactness" table's count and
+ * non-finite mask) on two more logit formats and for larger k.  The pages
+ * state it for bf16 with a max_k constant; the same order and readings hold
+ * here: NaN is never selected, +0 and -0 tie, infinities are ordinary
+ * extreme scores, subnormals are exact, and empty slots hold index -1 and the
+ * format's quiet NaN (bf16 0x7FC0, fp16 0x7E00, fp32 0x7FC00000).
+ *
+ *   logits       device, rows x row_stride elements of `dtype`
+ *                (TF_TOPK_DTYPE_*), aligned to the element size; columns
+ *                [cols, row_stride) are never read.
+ *   k            1..TF_TOPK_MAX_K_WIDE; k > cols is allowed.
+ *   out_idx      device int32 [rows][k]; out_val device [rows][k] elements of
+ *                `dtype` (the original bits); out_count int32 [rows];
+ *                out_nonfinite_mask uint32 [rows] (1 NaN, 2 +inf, 4 -inf).
+ * bf16 with k <= TF_TOPK_MAX_K runs the plans of tf_topk_bf16 (the same
+ * results, byte for byte); everything else runs the wide kernel: one CTA per
+ * row, two passes over the row (a bound from each thread's four best keys,
+ * then every element reaching it, sorted), with an exact counting search
+ * when ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
+ * Returns a TF_TOPK_* status: ERR_DTYPE for an unknown format, ERR_K,
+ * ERR_SHAPE, ERR_NULL, ERR_ALIGN as for tf_topk_bf16.
+ */
+#define TF_TOPK_MAX_K_WIDE 1024
+#define TF_TOPK_DTYPE_BF16 0
+#define TF_TOPK_DTYPE_F16 1
+#define TF_TOPK_DTYPE_F32 2
+#define TF_TOPK_PLAN_WIDE 64 /* tf_topk_select_with_plan: the wide kernel for any format and k */
+#define TF_TOPK_ERR_DTYPE 10 /* tf_topk_select: unknown logit format */
+int tf_topk_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                   int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream);
+
+/* tf_topk_select with a plan: TF_TOPK_PLAN_AUTO, TF_TOPK_PLAN_WIDE, or (bf16
+ * with k <= TF_TOPK_MAX_K only) a plan of tf_topk_bf16_with_plan; anything
+ * else returns TF_TOPK_ERR_PLAN. */
+int tf_topk_select_with_plan(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride,
+                             int32_t k, int32_t *out_idx, void *out_val, int32_t *out_count,
+                             uint32_t *out_nonfinite_mask, int32_t plan, void *stream);
+int32_t tf_topk_select_max_k(void); /* == TF_TOPK_MAX_K_WIDE */
+
 /* Human-readable text for a TF_TOPK_* status (static storage). */
 const char *tf_topk_strerror(int status);
 

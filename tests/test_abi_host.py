@@ -99,8 +99,8 @@ def test_zero_rows_is_a_no_op(lib):
 
 def test_strerror_covers_every_status(lib):
     from wide_bf16_row_gb300 import topk
-    texts = {topk.strerror(s) for s in range(10)}
-    assert len(texts) == 10 and "unknown status" not in texts
+    texts = {topk.strerror(s) for s in range(11)}
+    assert len(texts) == 11 and "unknown status" not in texts
     assert topk.strerror(99) == "unknown status"
 
 
@@ -170,3 +170,34 @@ def test_nucleus_guards_reject_before_launch(lib, kwargs, status):
 def test_nucleus_zero_rows_is_a_no_op(lib):
     assert nucleus_call(lib, rows=0, val=None, count=None, prob=None, keep=None) == 0
     assert nucleus_call(lib, rows=0, temperature=0.0, top_p=1.0) == 0
+
+
+def select_call(lib, dtype=0, rows=4, cols=100, stride=100, k=8, logits=FAKE, idx=FAKE, val=FAKE, count=FAKE,
+                mask=FAKE, plan=0):
+    from wide_bf16_row_gb300 import topk
+    return topk.tf_topk_select_with_plan(logits, dtype, rows, cols, stride, k, idx, val, count, mask, plan, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(dtype=3), 10), (dict(dtype=-1), 10),
+    (dict(k=0), 3), (dict(k=1025), 3), (dict(dtype=2, k=1025), 3),
+    (dict(rows=-1), 2), (dict(cols=0), 2), (dict(stride=99), 2),
+    (dict(dtype=1, plan=2), 5), (dict(k=65, plan=2), 5), (dict(plan=3), 5), (dict(dtype=2, plan=32), 5),
+    (dict(logits=None), 1), (dict(idx=None), 1), (dict(val=None), 1), (dict(count=None), 1), (dict(mask=None), 1),
+    (dict(logits=FAKE + 1), 4), (dict(dtype=2, logits=FAKE + 2), 4), (dict(dtype=2, val=FAKE + 2), 4),
+    (dict(dtype=1, val=FAKE + 1), 4), (dict(idx=FAKE + 2), 4),
+])
+def test_select_guards_reject_before_launch(lib, kwargs, status):
+    """tf_topk_select checks its arguments before any CUDA work."""
+    assert select_call(lib, **kwargs) == status
+
+
+def test_select_zero_rows_and_constants(lib):
+    from wide_bf16_row_gb300 import topk
+    assert select_call(lib, rows=0, logits=None, idx=None, val=None, count=None, mask=None) == 0
+    assert select_call(lib, rows=0, dtype=2, k=1024, plan=64) == 0
+    macros = header_macros()
+    assert topk.library().tf_topk_select_max_k() == macros["TF_TOPK_MAX_K_WIDE"] == 1024
+    assert (macros["TF_TOPK_DTYPE_BF16"], macros["TF_TOPK_DTYPE_F16"], macros["TF_TOPK_DTYPE_F32"]) == \
+        (topk.DTYPE_BF16, topk.DTYPE_F16, topk.DTYPE_F32)
+    assert macros["TF_TOPK_PLAN_WIDE"] == topk.PLAN_WIDE and macros["TF_TOPK_ERR_DTYPE"] == topk.ERR_DTYPE

@@ -1,0 +1,153 @@
+"""GPU parity of tf_topk_select -- bf16, fp16 and fp32 rows, k up to 1024 --
+against the CPU oracle, byte for byte (the order of TensorFold PR #713,
+change 3, and the "Exactness" table's count and mask, applied to the two
+further formats and to larger k).
+
+Cases: every format over k from 1 to 1024; padded strides and row bases off
+the 16-byte grid (the unaligned head and tail); rows shorter than k; the
+heavy-tie fallback (all +-0, few distinct values, a k-th key shared by
+thousands of columns); all-NaN rows; fp32 near-ties in the low half; the
+256 x 248320 bench shape forced through the wide kernel; and bf16 with
+k <= 64 through tf_topk_select against tf_topk_bf16."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from wide_bf16_row_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+CODES = {"bf16": 0, "f16": 1, "f32": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from wide_bf16_row_gb300 import build
+    build.build()
+
+
+def _device(x: np.ndarray, cols: int, offset: int = 0):
+    """(rows, cols) CUDA view of x (rows x stride bits) starting `offset` elements into a buffer."""
+    import torch
+
+    rows, stride = x.shape
+    sint = np.int32 if x.dtype == np.uint32 else np.int16
+    flat = torch.zeros(offset + rows * stride + 8, dtype=torch.int32 if sint is np.int32 else torch.int16,
+                       device="cuda")
+    flat[offset: offset + rows * stride] = torch.from_numpy(np.ascontiguousarray(x).view(sint).ravel()).cuda()
+    return flat.as_strided((rows, cols), (stride, 1), offset), flat
+
+
+def gpu_select(x: np.ndarray, cols: int, k: int, dtype: str, plan: int = 0, offset: int = 0):
+    import torch
+
+    from wide_bf16_row_gb300 import topk
+
+    view, hold = _device(x, cols, offset)
+    idx, val, count, mask = topk.select_topk(view, k, dtype=CODES[dtype], plan=plan)
+    torch.cuda.synchronize()
+    bits = np.uint32 if dtype == "f32" else np.uint16
+    out = (idx.cpu().numpy(), val.cpu().numpy().view(bits), count.cpu().numpy(), mask.cpu().numpy().view(np.uint32))
+    del hold
+    return out
+
+
+def assert_same(got, exp, what):
+    for g, e, name in zip(got, exp, ("idx", "val", "count", "mask")):
+        if not np.array_equal(g, e):
+            bad = np.argwhere(g != e)
+            first = tuple(bad[0])
+            raise AssertionError(f"{what}: {name} differs at {len(bad)} places, first {first}: "
+                                 f"got {g[first]} expected {e[first]}")
+
+
+def gen(dtype: str, rows: int, cols: int, seed: int, stride: int | None = None, **kw):
+    if dtype == "bf16":
+        return synth.mixed_rows(rows, cols, seed=seed, row_stride=stride, **kw)
+    if dtype == "f16":
+        return synth.mixed_rows_f16(rows, cols, seed=seed, row_stride=stride, **kw)
+    return synth.mixed_rows_f32(rows, cols, seed=seed, row_stride=stride, **kw)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("k", [1, 20, 64, 65, 256, 1024])
+def test_formats_and_k(dtype, k):
+    """Mixed rows (specials, copies, subnormals) at several widths, padded strides."""
+    for rows, cols, stride, seed in ((7, 5000, 5003, 1), (3, 70001, 70016, 2), (2, 700, 700, 3)):
+        x = gen(dtype, rows, cols, seed + 10 * k, stride, special_frac=0.03, dup_frac=0.05)
+        exp = oracle.topk(x, cols, k, dtype=dtype)
+        assert_same(gpu_select(x, cols, k, dtype, plan=64), exp, f"{dtype} k{k} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("offset", [1, 3, 5])
+def test_unaligned_row_bases(dtype, offset):
+    x = gen(dtype, 5, 3001, 40 + offset, 3011, special_frac=0.05)
+    for k in (7, 300):
+        assert_same(gpu_select(x, 3001, k, dtype, plan=64, offset=offset), oracle.topk(x, 3001, k, dtype=dtype),
+                    f"{dtype} offset {offset} k{k}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_heavy_ties_take_the_exact_path(dtype):
+    """More than 4096 columns reach the bound: all +-0 rows, three distinct
+    values, a k-th key shared by thousands; plus all-NaN and short rows."""
+    rng = np.random.default_rng(7)
+    cols = 20000
+    bits = np.uint32 if dtype == "f32" else np.uint16
+    sign = (1 << 31) if dtype == "f32" else (1 << 15)
+    one = {"bf16": 0x3F80, "f16": 0x3C00, "f32": 0x3F800000}[dtype]
+    two = {"bf16": 0x4000, "f16": 0x4000, "f32": 0x40000000}[dtype]
+    nan = {"bf16": 0x7FC0, "f16": 0x7E00, "f32": 0x7FC00000}[dtype]
+    x = np.zeros((6, cols), bits)
+    x[0] = rng.integers(0, 2, size=cols).astype(bits) * bits(sign)          # +-0 only
+    x[1] = rng.choice(np.array([one, two, one | sign], bits), size=cols)      # three values
+    x[2] = np.where(rng.random(cols) < 0.001, two, one).astype(bits)          # few 2.0, many 1.0
+    x[3] = nan                                                                # all NaN
+    x[4] = nan
+    x[4, ::4000] = one                                                        # five numbers
+    x[5] = rng.integers(0, 2, size=cols).astype(bits) * bits(sign)
+    x[5, 100:110] = two
+    for k in (1, 33, 64, 500, 1024):
+        assert_same(gpu_select(x, cols, k, dtype, plan=64), oracle.topk(x, cols, k, dtype=dtype),
+                    f"{dtype} ties k{k}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_rows_shorter_than_k(dtype):
+    x = gen(dtype, 9, 37, 5, 40, special_frac=0.2)
+    for k in (36, 37, 38, 1024):
+        assert_same(gpu_select(x, 37, k, dtype, plan=64), oracle.topk(x, 37, k, dtype=dtype), f"{dtype} k{k}")
+
+
+def test_bench_shape_through_the_wide_kernel():
+    w = synth.config_draft_window()
+    exp = oracle.topk(w.logits, w.cols, w.k)
+    assert_same(gpu_select(w.logits, w.cols, w.k, "bf16", plan=64), exp, "256x248320 wide")
+    for k in (100, 1024):
+        exp = oracle.topk(w.logits[:16], w.cols, k)
+        assert_same(gpu_select(w.logits[:16], w.cols, k, "bf16", plan=64), exp, f"16x248320 k{k}")
+
+
+def test_specials_config_all_formats():
+    """16 x 248320 with NaN, infinities, zeros, an all-NaN and an all-zero row (bf16),
+    and fp16/fp32 rows of the same width."""
+    w = synth.config_specials()
+    assert_same(gpu_select(w.logits, w.cols, 300, "bf16", plan=64), oracle.topk(w.logits, w.cols, 300),
+                "specials bf16 k300")
+    for dtype in ("f16", "f32"):
+        x = gen(dtype, 6, 248320, 77, 248384, special_frac=0.01, dup_frac=0.01)
+        for k in (20, 1024):
+            assert_same(gpu_select(x, 248320, k, dtype), oracle.topk(x, 248320, k, dtype=dtype),
+                        f"{dtype} 248320 k{k}")
+
+
+def test_bf16_small_k_matches_tf_topk_bf16():
+    """tf_topk_select on bf16 with k <= 64 runs the tf_topk_bf16 plans: same bytes."""
+    from tests.gpu_util import gpu_topk
+    w = synth.config_draft_head()
+    for plan in (0, 2, 8):
+        got = gpu_select(w.logits, w.cols, w.k, "bf16", plan=plan)
+        assert_same(got, gpu_topk(w.logits, w.cols, w.k, plan=plan), f"select plan {plan}")

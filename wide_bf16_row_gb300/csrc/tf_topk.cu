@@ -59,6 +59,7 @@
 #include <mutex>
 #include <thread>
 
+#include <type_traits>
 #include <utility>
 
 #include "tf_topk.h"
@@ -1598,6 +1599,460 @@ topk_nucleus_kernel(const uint16_t *__restrict__ val, const int32_t *__restrict_
     if (lane == 0) out_keep[r] = keep;
 }
 
+// ------------------------------------------------ wide select: any format, k <= 1024
+//
+// The same order (score descending, lower column first; NaN never selected,
+// +0 == -0) for bf16, fp16 and fp32 rows and k up to TF_TOPK_MAX_K_WIDE.  One
+// CTA per row, in two passes over the row:
+//   1. each thread keeps the keys of its Q best elements (distinct elements;
+//      Q = 4, or 16 for k > 256), and the CTA takes the row's non-finite mask
+//      and its count of numbers.  Each warp finds the j-th largest of its
+//      lanes' kept keys, j = ceil(k / warps), so B = the smallest of those is
+//      reached by at least k elements of the row;
+//   2. every element with key >= B -- a superset of the row's top k, ties at
+//      B included -- goes into shared memory as a 64-bit entry (key << 32 |
+//      ~column); ranking them (by count, or a bitonic sort when many) gives
+//      the order (equal keys: the higher ~column, i.e. the lower column,
+//      first), of which the first k are the result.
+// When more than kWideCap elements reach B (heavy ties), the k-th key K* is
+// found exactly by a 16-ary search over counting passes, the entries above it
+// are collected, and the ties at K* are taken in column order from
+// contiguous per-thread column ranges.
+
+constexpr int kWideThreads = 256;
+constexpr int kWideWarps = kWideThreads / 32;
+constexpr int kWideUnroll = 8;                  // 16-byte loads in flight per thread
+constexpr int kWideCap = 4096;                  // entries pass 2 may collect
+constexpr int kWideMaxK = TF_TOPK_MAX_K_WIDE;
+constexpr int kWideSmallK = 256;                // k up to this keeps 4 keys a thread, above it 16
+static_assert(32 * 4 >= (kWideSmallK + kWideWarps - 1) / kWideWarps, "a warp keeps j keys (small k)");
+static_assert(32 * 16 >= (kWideMaxK + kWideWarps - 1) / kWideWarps, "a warp keeps j keys (large k)");
+static_assert(kWideCap >= kWideMaxK, "a short row's numbers all fit");
+
+// Order-preserving key of one element (0 for NaN, +0 and -0 one key), and
+// its non-finite flag (1 NaN, 2 +inf, 4 -inf).
+template <typename T, int kFmt>
+struct WideFormat;
+
+template <>
+struct WideFormat<uint16_t, TF_TOPK_DTYPE_BF16> {
+    static constexpr uint32_t kNanFloor = 0x7F80u, kPosInf = 0x7F80u, kNegInf = 0xFF80u, kEmpty = 0x7FC0u;
+    static constexpr uint32_t kSign = 0x8000u, kOnes = 0xFFFFu;
+};
+template <>
+struct WideFormat<uint16_t, TF_TOPK_DTYPE_F16> {
+    static constexpr uint32_t kNanFloor = 0x7C00u, kPosInf = 0x7C00u, kNegInf = 0xFC00u, kEmpty = 0x7E00u;
+    static constexpr uint32_t kSign = 0x8000u, kOnes = 0xFFFFu;
+};
+template <>
+struct WideFormat<uint32_t, TF_TOPK_DTYPE_F32> {
+    static constexpr uint32_t kNanFloor = 0x7F800000u, kPosInf = 0x7F800000u, kNegInf = 0xFF800000u,
+                              kEmpty = 0x7FC00000u;
+    static constexpr uint32_t kSign = 0x80000000u, kOnes = 0xFFFFFFFFu;
+};
+
+// Keys of the infinities: a raw key (sign-flipped bits, NaN not yet zeroed)
+// above the +inf key or below the -inf key is a NaN.
+template <typename T, int kFmt>
+struct WideKeys {
+    using F = WideFormat<T, kFmt>;
+    static constexpr uint32_t kPosInfKey = F::kPosInf ^ F::kSign;
+    static constexpr uint32_t kNegInfKey = F::kNegInf ^ F::kOnes;
+};
+
+// Raw keys of a 16-byte vector, one 32-bit word at a time: two 16-bit keys
+// per word (packed), or one 32-bit key.
+__device__ __forceinline__ uint32_t raw_key_word(uint32_t w, std::integral_constant<int, 2>)
+{
+    return keys_from_raw2(w);
+}
+__device__ __forceinline__ uint32_t raw_key_word(uint32_t w, std::integral_constant<int, 4>)
+{
+    return w ^ ((uint32_t)((int32_t)w >> 31) | 0x80000000u);
+}
+
+template <typename T, int kFmt>
+__device__ __forceinline__ uint32_t wide_key(uint32_t raw)
+{
+    using F = WideFormat<T, kFmt>;
+    if ((raw & ~F::kSign) > F::kNanFloor) return 0u;             // NaN
+    const uint32_t key = raw ^ ((raw & F::kSign) ? F::kOnes : F::kSign);
+    return key == F::kSign - 1u ? F::kSign : key;                  // -0 -> +0
+}
+
+template <typename T, int kFmt>
+__device__ __forceinline__ uint32_t wide_flag(uint32_t raw)
+{
+    using F = WideFormat<T, kFmt>;
+    if ((raw & ~F::kSign) > F::kNanFloor) return 1u;
+    if (raw == F::kPosInf) return 2u;
+    if (raw == F::kNegInf) return 4u;
+    return 0u;
+}
+
+// Every column of the row, each thread a strided share: the row's unaligned
+// head and tail through f(column, raw bits), the 16-byte-aligned body
+// through g(vector, its first column), kWideUnroll vectors a thread in flight
+// before any is used.  With kEdges false only the body is visited.
+template <typename T, bool kEdges, typename Fe, typename Fv>
+__device__ __forceinline__ void wide_scan2(const T *row, int32_t cols, Fe &&f, Fv &&g)
+{
+    constexpr int kPer = 16 / (int)sizeof(T);
+    const int tid = threadIdx.x;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    int32_t head = (int32_t)(((16u - (uint32_t)(a & 15u)) & 15u) / sizeof(T));
+    if (head > cols) head = cols;
+    if constexpr (kEdges)
+        for (int32_t c = tid; c < head; c += kWideThreads) f(c, (uint32_t)row[c]);
+    const int32_t nvec = (cols - head) / kPer;
+    const uint4 *v = reinterpret_cast<const uint4 *>(row + head);
+    int32_t i = tid;
+    for (; i + (kWideUnroll - 1) * kWideThreads < nvec; i += kWideUnroll * kWideThreads) {
+        uint4 q[kWideUnroll];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) q[u] = v[i + u * kWideThreads];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) g(q[u], head + (i + u * kWideThreads) * kPer);
+    }
+    for (; i < nvec; i += kWideThreads) g(v[i], head + i * kPer);
+    if constexpr (kEdges)
+        for (int32_t c = head + nvec * kPer + tid; c < cols; c += kWideThreads) f(c, (uint32_t)row[c]);
+}
+
+// The elements of a vector, in column order: f(column, raw bits).
+template <typename T, typename Fe>
+__device__ __forceinline__ void vector_elems(const uint4 &q, int32_t c0, Fe &&f)
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (sizeof(T) == 2) {
+            f(c0 + 2 * j, w[j] & 0xFFFFu);
+            f(c0 + 2 * j + 1, w[j] >> 16);
+        } else {
+            f(c0 + j, w[j]);
+        }
+    }
+}
+
+// f(column, raw bits) for every column of the row.
+template <typename T, typename Fe>
+__device__ __forceinline__ void wide_scan(const T *row, int32_t cols, Fe &&f)
+{
+    wide_scan2<T, true>(row, cols, f, [&](const uint4 &q, int32_t c0) { vector_elems<T>(q, c0, f); });
+}
+
+// Max and min raw key of a vector (16-bit keys packed in pairs).
+template <typename T>
+__device__ __forceinline__ void vector_key_range(const uint4 &q, uint32_t &vmx, uint32_t &vmn)
+{
+    constexpr std::integral_constant<int, (int)sizeof(T)> width{};
+    const uint32_t a = raw_key_word(q.x, width), b = raw_key_word(q.y, width);
+    const uint32_t c = raw_key_word(q.z, width), d = raw_key_word(q.w, width);
+    if constexpr (sizeof(T) == 2) {
+        vmx = max_u16x2(max_u16x2(a, b), max_u16x2(c, d));
+        vmn = min_u16x2(min_u16x2(a, b), min_u16x2(c, d));
+    } else {
+        vmx = max(max(a, b), max(c, d));
+        vmn = min(min(a, b), min(c, d));
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t hi_key(uint32_t packed)
+{
+    if constexpr (sizeof(T) == 2) return max(packed & 0xFFFFu, packed >> 16);
+    else return packed;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t lo_key(uint32_t packed)
+{
+    if constexpr (sizeof(T) == 2) return min(packed & 0xFFFFu, packed >> 16);
+    else return packed;
+}
+
+// Descending bitonic sort of s[0..n) (n a power of two), every thread of the
+// CTA taking part; ends with a barrier.
+template <typename K>
+__device__ __forceinline__ void bitonic_desc(K *s, int n)
+{
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < (n >> 1); i += kWideThreads) {
+                const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                const bool desc = (lo & size) == 0;
+                const K x = s[lo], y = s[hi];
+                if ((x < y) == desc) {
+                    s[lo] = y;
+                    s[hi] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t wide_block_sum(uint32_t v, uint32_t *red)
+{
+    v = __reduce_add_sync(0xFFFFFFFFu, v);
+    __syncthreads(); // red is free (an earlier sum has been read)
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t s = 0;
+#pragma unroll
+    for (int w = 0; w < kWideThreads / 32; ++w) s += red[w];
+    return s;
+}
+
+struct __align__(16) WideSmem {
+    uint64_t ent[kWideCap];
+    uint64_t sorted[kWideThreads];           // ranked entries when few
+    uint32_t red[kWideWarps];
+    uint32_t warp_b[kWideWarps];
+    uint32_t n_ent, flags, nnz, kmax;
+};
+
+// Keep the Q largest keys seen (t[0] >= ... >= t[Q-1]; 0 = empty).
+template <int Q>
+__device__ __forceinline__ void keep_insert(uint32_t (&t)[Q], uint32_t key)
+{
+    if (key > t[Q - 1]) {
+        t[Q - 1] = key;
+#pragma unroll
+        for (int i = Q - 1; i > 0; --i) {
+            const uint32_t a = t[i - 1], b = t[i];
+            t[i - 1] = max(a, b);
+            t[i] = min(a, b);
+        }
+    }
+}
+
+// The j-th largest of the warp's kept keys (lanes' lists sorted, popped from
+// the head), or 0 when the warp holds fewer than j nonzero keys.  Warp-uniform.
+template <int Q>
+__device__ __forceinline__ uint32_t warp_jth(uint32_t (&t)[Q], uint32_t j)
+{
+    uint32_t cnt = 0;
+    for (uint32_t it = 0; it < j; ++it) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, t[0]);
+        if (m == 0) return 0;
+        cnt += __popc(__ballot_sync(0xFFFFFFFFu, t[0] == m));
+        if (cnt >= j) return m;
+        if (t[0] == m) {
+#pragma unroll
+            for (int i = 0; i < Q - 1; ++i) t[i] = t[i + 1];
+            t[Q - 1] = 0;
+        }
+    }
+    return 0; // not reached: every step pops at least one key
+}
+
+template <typename T, int kFmt, int Q>
+__global__ void __launch_bounds__(kWideThreads)
+topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
+                 int32_t *__restrict__ out_idx, T *__restrict__ out_val, int32_t *__restrict__ out_count,
+                 uint32_t *__restrict__ out_mask)
+{
+    using F = WideFormat<T, kFmt>;
+    extern __shared__ __align__(16) unsigned char wide_dsmem[];
+    WideSmem &sm = *reinterpret_cast<WideSmem *>(wide_dsmem);
+    const int tid = threadIdx.x;
+    const int64_t r = blockIdx.x;
+    const T *row = logits + r * row_stride;
+    grid_dependency_wait();
+    if (tid == 0) {
+        sm.n_ent = 0;
+        sm.flags = 0;
+        sm.nnz = 0;
+        sm.kmax = 0;
+    }
+
+    // ---- pass 1: each thread's Q best keys, the mask, the count of numbers.
+    // A vector's elements are looked at one by one only when its max raw key
+    // passes the thread's kept floor; the mask and the NaN count come from a
+    // second look at the thread's vectors, taken only when its raw keys reached
+    // an infinity's.
+    using FK = WideKeys<T, kFmt>;
+    uint32_t t[Q];
+#pragma unroll
+    for (int i = 0; i < Q; ++i) t[i] = 0;
+    uint32_t flags = 0, nnz = 0, smx = 0, smn = 0xFFFFFFFFu, nv = 0;
+    auto elem1 = [&](int32_t, uint32_t raw) {
+        const uint32_t key = wide_key<T, kFmt>(raw);
+        flags |= wide_flag<T, kFmt>(raw);
+        nnz += key != 0u;
+        keep_insert<Q>(t, key);
+    };
+    wide_scan2<T, true>(row, cols, elem1, [&](const uint4 &q, int32_t) {
+        uint32_t vmx, vmn;
+        vector_key_range<T>(q, vmx, vmn);
+        if constexpr (sizeof(T) == 2) {
+            smx = max_u16x2(smx, vmx);
+            smn = min_u16x2(smn, vmn);
+        } else {
+            smx = max(smx, vmx);
+            smn = min(smn, vmn);
+        }
+        ++nv;
+        if (hi_key<T>(vmx) > t[Q - 1])
+            vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
+    });
+    uint32_t nan = 0;
+    if (hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey) {
+        wide_scan2<T, false>(row, cols, elem1, [&](const uint4 &q, int32_t) {
+            vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) {
+                flags |= wide_flag<T, kFmt>(raw);
+                nan += wide_key<T, kFmt>(raw) == 0u;
+            });
+        });
+    }
+    nnz += nv * (16u / (uint32_t)sizeof(T)) - nan;
+    flags = __reduce_or_sync(0xFFFFFFFFu, flags);
+    nnz = __reduce_add_sync(0xFFFFFFFFu, nnz);
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, t[0]);
+    const uint32_t jth = warp_jth<Q>(t, (uint32_t)((k + kWideWarps - 1) / kWideWarps));
+    __syncthreads(); // the initialisation above is visible
+    if ((tid & 31) == 0) {
+        atomicOr(&sm.flags, flags);
+        atomicAdd(&sm.nnz, nnz);
+        atomicMax(&sm.kmax, wmax);
+        sm.warp_b[tid >> 5] = jth;
+    }
+    __syncthreads();
+    const uint32_t total = sm.nnz;
+    const int cnt = (int)min((uint32_t)k, total);
+    // each warp holds j elements at or above its j-th key, and warps * j >= k:
+    // k elements reach the smallest (every number does, when a warp ran out)
+    uint32_t bound = 0xFFFFFFFFu;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) bound = min(bound, sm.warp_b[w]);
+    bound = max(bound, 1u);
+    const uint32_t kmax = sm.kmax;
+
+    // ---- pass 2: every element reaching the bound (vectors below it skipped
+    // whole; -0's raw key sits just below +0's)
+    const uint32_t vfloor = bound == F::kSign ? bound - 1u : bound;
+    auto elem2 = [&](int32_t c, uint32_t raw) {
+        const uint32_t key = wide_key<T, kFmt>(raw);
+        if (key >= bound) {
+            const uint32_t slot = atomicAdd(&sm.n_ent, 1u);
+            if (slot < (uint32_t)kWideCap) sm.ent[slot] = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)c);
+        }
+    };
+    wide_scan2<T, true>(row, cols, elem2, [&](const uint4 &q, int32_t c0) {
+        uint32_t vmx, vmn;
+        vector_key_range<T>(q, vmx, vmn);
+        if (hi_key<T>(vmx) >= vfloor) vector_elems<T>(q, c0, elem2);
+    });
+    __syncthreads();
+    const uint32_t n = sm.n_ent;
+    const uint64_t *res = sm.ent;
+    if (n <= (uint32_t)kWideThreads) {
+        // few: an entry's place is the number of larger entries (all distinct)
+        if (tid < (int)n) {
+            const uint64_t x = sm.ent[tid];
+            uint32_t rank = 0;
+            for (uint32_t u = 0; u < n; ++u) rank += sm.ent[u] > x;
+            sm.sorted[rank] = x;
+        }
+        __syncthreads();
+        res = sm.sorted;
+    } else if (n <= (uint32_t)kWideCap) {
+        int pn = 1;
+        while (pn < (int)n) pn <<= 1;
+        for (int i = (int)n + tid; i < pn; i += kWideThreads) sm.ent[i] = 0; // pads sort last
+        __syncthreads();
+        bitonic_desc(sm.ent, pn);
+    } else {
+        __syncthreads(); // every thread has read n before n_ent is reused below
+        // ---- heavy ties: K* by a 16-ary search on counts, kmax + 1 counts 0
+        uint64_t lo = bound, hi = (uint64_t)kmax + 1u; // count(>= lo) >= k > count(>= hi)
+        while (hi - lo > 1) {
+            const uint64_t step = (hi - lo + 15) / 16;
+            uint32_t c[15];
+#pragma unroll
+            for (int j = 0; j < 15; ++j) c[j] = 0;
+            wide_scan(row, cols, [&](int32_t, uint32_t raw) {
+                const uint64_t key = wide_key<T, kFmt>(raw);
+#pragma unroll
+                for (int j = 0; j < 15; ++j) c[j] += key >= lo + (uint64_t)(j + 1) * step;
+            });
+            uint64_t nlo = lo, nhi = hi;
+            for (int j = 0; j < 15; ++j) {
+                const uint64_t t = lo + (uint64_t)(j + 1) * step;
+                const uint32_t cj = wide_block_sum(c[j], sm.red); // every thread, every j
+                if (t < hi) {
+                    if (cj >= (uint32_t)k) nlo = t;
+                    else if (t < nhi) nhi = t;
+                }
+            }
+            lo = nlo;
+            hi = nhi;
+        }
+        const uint32_t kstar = (uint32_t)lo;
+        // entries above K*: fewer than k, any order
+        if (tid == 0) sm.n_ent = 0;
+        __syncthreads();
+        wide_scan(row, cols, [&](int32_t c, uint32_t raw) {
+            const uint32_t key = wide_key<T, kFmt>(raw);
+            if (key > kstar) {
+                const uint32_t slot = atomicAdd(&sm.n_ent, 1u);
+                sm.ent[slot] = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)c);
+            }
+        });
+        __syncthreads();
+        const uint32_t above = sm.n_ent;
+        const uint32_t need = (uint32_t)k - above;
+        // ties at K* in column order: each thread a contiguous column range
+        const int32_t span = (cols + kWideThreads - 1) / kWideThreads;
+        const int32_t c0 = min(cols, tid * span), c1 = min(cols, c0 + span);
+        uint32_t ties = 0;
+        for (int32_t c = c0; c < c1; ++c) ties += wide_key<T, kFmt>((uint32_t)row[c]) == kstar;
+        // exclusive scan of ties over threads (thread order = column order)
+        const int lane = tid & 31, warp = tid >> 5;
+        uint32_t incl = ties;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += u;
+        }
+        __syncthreads();
+        if (lane == 31) sm.red[warp] = incl;
+        __syncthreads();
+        uint32_t rank = incl - ties;
+        for (int w = 0; w < warp; ++w) rank += sm.red[w];
+        for (int32_t c = c0; c < c1 && rank < need; ++c) {
+            if (wide_key<T, kFmt>((uint32_t)row[c]) == kstar) {
+                sm.ent[above + rank] = ((uint64_t)kstar << 32) | (uint64_t)(~(uint32_t)c);
+                ++rank;
+            }
+        }
+        __syncthreads();
+        int pn = 1;
+        while (pn < k) pn <<= 1;
+        for (int i = k + tid; i < pn; i += kWideThreads) sm.ent[i] = 0;
+        __syncthreads();
+        bitonic_desc(sm.ent, pn);
+    }
+
+    // ---- the row: the first cnt entries, original bits re-read by column
+    for (int i = tid; i < k; i += kWideThreads) {
+        if (i < cnt) {
+            const int32_t c = (int32_t)(~(uint32_t)res[i]);
+            out_idx[r * k + i] = c;
+            out_val[r * k + i] = row[c];
+        } else {
+            out_idx[r * k + i] = -1;
+            out_val[r * k + i] = (T)F::kEmpty;
+        }
+    }
+    if (tid == 0) {
+        out_count[r] = cnt;
+        out_mask[r] = sm.flags;
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 constexpr size_t kStreamSmemBytes =
@@ -2014,6 +2469,93 @@ int run_nucleus(const uint16_t *val, const int32_t *count, int64_t rows, int32_t
     return TF_TOPK_OK;
 }
 
+// tf_topk_select with the wide kernel: one CTA per row, in blocks of at most
+// 2^31 - 1 rows per launch.
+template <typename T, int kFmt, int Q>
+int launch_wide(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k, int32_t *out_idx,
+                void *out_val, int32_t *out_count, uint32_t *out_mask, cudaStream_t strm)
+{
+    static bool attr_done[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (!attr_done[dev]) {
+        e = cudaFuncSetAttribute(topk_wide_kernel<T, kFmt, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(WideSmem));
+        if (e != cudaSuccess) return fail_cuda(e);
+        attr_done[dev] = true;
+    }
+    const T *x = static_cast<const T *>(logits);
+    T *ov = static_cast<T *>(out_val);
+    const int64_t max_rows = (int64_t)INT32_MAX;
+    for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
+        const int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nr, 1, 1);
+        cfg.blockDim = dim3(kWideThreads, 1, 1);
+        cfg.dynamicSmemBytes = sizeof(WideSmem);
+        cfg.stream = strm;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, topk_wide_kernel<T, kFmt, Q>, x + r0 * row_stride, (int32_t)cols, row_stride, k,
+                               out_idx + r0 * k, ov + r0 * k, out_count + r0, out_mask + r0);
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return TF_TOPK_OK;
+}
+
+// tf_topk_select / tf_topk_select_with_plan: guards, then bf16 with k <= 64 on
+// the fast plans (AUTO unless a plan is named), everything else on the wide
+// kernel.
+int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+               int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_mask, int32_t plan, void *stream)
+{
+    if (dtype != TF_TOPK_DTYPE_BF16 && dtype != TF_TOPK_DTYPE_F16 && dtype != TF_TOPK_DTYPE_F32)
+        return TF_TOPK_ERR_DTYPE;
+    if (k < 1 || k > kWideMaxK) return TF_TOPK_ERR_K;
+    if (rows < 0 || cols < 1 || row_stride < cols || cols > (int64_t)INT32_MAX - 64) return TF_TOPK_ERR_SHAPE;
+    if (rows > 0 && row_stride > INT64_MAX / rows) return TF_TOPK_ERR_SHAPE;
+    if (plan != TF_TOPK_PLAN_AUTO && plan != TF_TOPK_PLAN_WIDE &&
+        (dtype != TF_TOPK_DTYPE_BF16 || k > kMaxK))
+        return TF_TOPK_ERR_PLAN; // the fast plans take bf16 with k <= 64 only
+    if (rows == 0) return TF_TOPK_OK;
+    if (!logits || !out_idx || !out_val || !out_count || !out_mask) return TF_TOPK_ERR_NULL;
+    const uintptr_t esz = dtype == TF_TOPK_DTYPE_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(logits) & (esz - 1)) || (reinterpret_cast<uintptr_t>(out_val) & (esz - 1)) ||
+        (reinterpret_cast<uintptr_t>(out_idx) & 3) || (reinterpret_cast<uintptr_t>(out_count) & 3) ||
+        (reinterpret_cast<uintptr_t>(out_mask) & 3))
+        return TF_TOPK_ERR_ALIGN;
+    if (dtype == TF_TOPK_DTYPE_BF16 && k <= kMaxK && plan != TF_TOPK_PLAN_WIDE)
+        return run(logits, rows, cols, row_stride, k, out_idx, static_cast<uint16_t *>(out_val), out_count,
+                   out_mask, plan, stream);
+    int dev = 0, sm_count = 0;
+    const int st = device_setup(&dev, &sm_count);
+    if (st != TF_TOPK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool small = k <= kWideSmallK;
+    switch (dtype) {
+    case TF_TOPK_DTYPE_BF16:
+        return small ? launch_wide<uint16_t, TF_TOPK_DTYPE_BF16, 4>(logits, rows, cols, row_stride, k, out_idx,
+                                                                    out_val, out_count, out_mask, s)
+                     : launch_wide<uint16_t, TF_TOPK_DTYPE_BF16, 16>(logits, rows, cols, row_stride, k, out_idx,
+                                                                     out_val, out_count, out_mask, s);
+    case TF_TOPK_DTYPE_F16:
+        return small ? launch_wide<uint16_t, TF_TOPK_DTYPE_F16, 4>(logits, rows, cols, row_stride, k, out_idx,
+                                                                   out_val, out_count, out_mask, s)
+                     : launch_wide<uint16_t, TF_TOPK_DTYPE_F16, 16>(logits, rows, cols, row_stride, k, out_idx,
+                                                                    out_val, out_count, out_mask, s);
+    default:
+        return small ? launch_wide<uint32_t, TF_TOPK_DTYPE_F32, 4>(logits, rows, cols, row_stride, k, out_idx,
+                                                                   out_val, out_count, out_mask, s)
+                     : launch_wide<uint32_t, TF_TOPK_DTYPE_F32, 16>(logits, rows, cols, row_stride, k, out_idx,
+                                                                    out_val, out_count, out_mask, s);
+    }
+}
+
 } // namespace
 
 extern "C" {
@@ -2057,6 +2599,21 @@ int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows
     return run_nucleus(val, count, rows, k, temperature, top_p, out_prob, out_keep, stream);
 }
 
+int tf_topk_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                   int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream)
+{
+    return run_select(logits, dtype, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask,
+                      TF_TOPK_PLAN_AUTO, stream);
+}
+
+int tf_topk_select_with_plan(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride,
+                             int32_t k, int32_t *out_idx, void *out_val, int32_t *out_count,
+                             uint32_t *out_nonfinite_mask, int32_t plan, void *stream)
+{
+    return run_select(logits, dtype, rows, cols, row_stride, k, out_idx, out_val, out_count, out_nonfinite_mask,
+                      plan, stream);
+}
+
 int32_t tf_topk_bf16_plan(int64_t rows, int64_t cols, int32_t k)
 {
     if (k < 1 || k > kMaxK) return -TF_TOPK_ERR_K;
@@ -2090,6 +2647,7 @@ int tf_topk_device_fault(void)
 }
 
 int32_t tf_topk_bf16_max_k(void) { return kMaxK; }
+int32_t tf_topk_select_max_k(void) { return kWideMaxK; }
 int32_t tf_topk_bf16_max_spans(void) { return kMaxSpans; }
 int32_t tf_topk_bf16_cta_threads(void) { return kThreads; }
 int32_t tf_topk_bf16_chunk_columns(void) { return kChunkCols; }
@@ -2106,6 +2664,7 @@ const char *tf_topk_strerror(int status)
     case TF_TOPK_ERR_DEVICE: return "current device is not compute capability 10.3 (sm_103a)";
     case TF_TOPK_ERR_CUDA: return "CUDA runtime error (see tf_topk_last_cuda_error)";
     case TF_TOPK_ERR_ARG: return "temperature or top_p out of range";
+    case TF_TOPK_ERR_DTYPE: return "unknown logit format (TF_TOPK_DTYPE_*)";
     case TF_TOPK_ERR_SCRATCH: return "the launch needs more scratch slots than the static area of "
                                      "tf_topk_bf16_noalloc holds (TF_TOPK_NOALLOC_MAX_CTAS)";
     default: return "unknown status";

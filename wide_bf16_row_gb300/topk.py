@@ -16,6 +16,9 @@ LIBRARY = PKG / "libtf_topk.so"
 OK, ERR_NULL, ERR_SHAPE, ERR_K, ERR_ALIGN, ERR_PLAN, ERR_DEVICE, ERR_CUDA = range(8)
 ERR_SCRATCH = 8  # tf_topk_bf16_noalloc only
 ERR_ARG = 9  # tf_topk_nucleus_bf16 only
+ERR_DTYPE = 10  # tf_topk_select only
+DTYPE_BF16, DTYPE_F16, DTYPE_F32 = 0, 1, 2
+PLAN_WIDE = 64  # tf_topk_select_with_plan: the wide kernel
 
 # launch plans (include/tf_topk.h)
 PLAN_AUTO, PLAN_SINGLE, PLAN_STREAM = 0, 1, 32
@@ -52,6 +55,13 @@ def library() -> ctypes.CDLL:
         lib.tf_topk_bf16_noalloc.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
         lib.tf_topk_nucleus_bf16.restype = ctypes.c_int
         lib.tf_topk_nucleus_bf16.argtypes = [c_p, c_p, c_i64, c_i32, ctypes.c_float, ctypes.c_float, c_p, c_p, c_p]
+        lib.tf_topk_select.restype = ctypes.c_int
+        lib.tf_topk_select.argtypes = [c_p, c_i32, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
+        lib.tf_topk_select_with_plan.restype = ctypes.c_int
+        lib.tf_topk_select_with_plan.argtypes = [c_p, c_i32, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p,
+                                                 c_i32, c_p]
+        lib.tf_topk_select_max_k.restype = c_i32
+        lib.tf_topk_select_max_k.argtypes = []
         lib.tf_topk_device_fault.restype = ctypes.c_int
         lib.tf_topk_device_fault.argtypes = []
         lib.tf_topk_bf16_plan.restype = c_i32
@@ -186,6 +196,60 @@ def nucleus_bf16(val, count, temperature: float, top_p: float, *, out=None, stre
         stream = torch.cuda.current_stream(val.device)
     _check(tf_topk_nucleus_bf16(val.data_ptr(), count.data_ptr(), rows, k, float(temperature), float(top_p),
                                 out[0].data_ptr(), out[1].data_ptr(), stream.cuda_stream))
+    return out
+
+
+def tf_topk_select(logits: int, dtype: int, rows: int, cols: int, row_stride: int, k: int, out_idx: int,
+                   out_val: int, out_count: int, out_nonfinite_mask: int, stream: int | None) -> int:
+    """The C entry point for bf16 / fp16 / fp32 rows and k up to 1024; returns the status code."""
+    return library().tf_topk_select(logits, dtype, rows, cols, row_stride, k, out_idx, out_val, out_count,
+                                    out_nonfinite_mask, stream)
+
+
+def tf_topk_select_with_plan(logits: int, dtype: int, rows: int, cols: int, row_stride: int, k: int,
+                             out_idx: int, out_val: int, out_count: int, out_nonfinite_mask: int, plan: int,
+                             stream: int | None) -> int:
+    """tf_topk_select with a plan (0 AUTO, PLAN_WIDE, or a bf16 plan for k <= 64)."""
+    return library().tf_topk_select_with_plan(logits, dtype, rows, cols, row_stride, k, out_idx, out_val,
+                                              out_count, out_nonfinite_mask, plan, stream)
+
+
+def select_topk(x, k: int, *, dtype: int | None = None, plan: int = 0, out=None, stream=None):
+    """Exact top-k of every row of a CUDA bf16 / fp16 / fp32 matrix, k up to 1024.
+
+    ``x``: bfloat16, float16 or float32 (or int16 / int32 holding the bits,
+    with ``dtype`` one of DTYPE_*), 1-D or 2-D with unit column stride.
+    Returns ``(idx int32[rows,k], val[rows,k] (x's dtype), count int32[rows],
+    mask int32[rows])``.
+    """
+    import torch
+
+    codes = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
+    if not x.is_cuda:
+        raise ValueError("select_topk needs a CUDA tensor (no CPU path exists)")
+    if dtype is None:
+        if x.dtype not in codes:
+            raise TypeError(f"pass dtype= for a {x.dtype} tensor of bits")
+        dtype = codes[x.dtype]
+    if x.element_size() != (4 if dtype == DTYPE_F32 else 2):
+        raise TypeError("element size does not match dtype")
+    if x.dim() == 1:
+        x = x.unsqueeze(0)
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("x must be 1-D or 2-D with contiguous columns")
+    rows, cols = x.shape
+    row_stride = x.stride(0) if rows > 1 else max(cols, x.stride(0))
+    dev = x.device
+    if out is None:
+        out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
+               torch.empty((rows, k), dtype=x.dtype, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev))
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    _check(tf_topk_select_with_plan(x.data_ptr(), dtype, rows, cols, row_stride, k, out[0].data_ptr(),
+                                    out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(), plan,
+                                    stream.cuda_stream))
     return out
 
 
