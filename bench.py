@@ -1,7 +1,7 @@
 """Benchmark: exact per-row bf16 top-k on GB300, one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--plan P]
+                    [--workload NAME] [--plan P] [--dtype bf16|f16|f32] [--k K]
 
 A step is one call of the whole path (load, key encode, span select, span
 merge, write) over one batch: the 256 x 248320 bf16 draft window with k = 20
@@ -14,6 +14,11 @@ the max over ranks.
 
 ``--impl reference`` times the CPU oracle (all host cores) on the same
 workload instead -- the reference arm; under torchrun only rank 0 runs it.
+
+``--dtype`` / ``--k`` time tf_topk_select on the same values in another
+format (fp32: the bf16 values widened exactly; fp16: rounded to nearest) or
+with another k; ``--plan 64`` forces its wide kernel.  The defaults are the
+bf16, k = 20 call above.
 """
 from __future__ import annotations
 
@@ -42,7 +47,12 @@ KERNEL_SOURCE = ROOT / "wide_bf16_row_gb300" / "csrc" / "tf_topk.cu"
 PROFILES = ROOT / "profiles"
 # the kernel each launch plan runs (the ncu summaries are named after it)
 PLAN_KERNEL = {1: "topk_stream_kernel_rowwise", 2: "topk_cluster_kernel_S2", 4: "topk_cluster_kernel_S4",
-               8: "topk_cluster_kernel_S8", 16: "topk_cluster_kernel_S16", 32: "topk_stream_kernel"}
+               8: "topk_cluster_kernel_S8", 16: "topk_cluster_kernel_S16", 32: "topk_stream_kernel",
+               64: "topk_wide_kernel"}
+PLAN_NAME = {1: "single", 2: "cluster2", 4: "cluster4", 8: "cluster8", 16: "cluster16", 32: "stream", 64: "wide"}
+# logit formats of tf_topk_select: (TF_TOPK_DTYPE_* code, bit-pattern type)
+FORMATS = {"bf16": (0, np.uint16), "f16": (1, np.uint16), "f32": (2, np.uint32)}
+FAST_MAX_K = 64
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -190,6 +200,25 @@ def make_workload(name: str, rank: int = 0):
     return synth.NAMED[name]()
 
 
+def format_bits(w, fmt: str) -> np.ndarray:
+    """The workload's values as bit patterns of `fmt`: bf16 as drawn, fp32
+    widened exactly, fp16 rounded to nearest."""
+    if fmt == "bf16":
+        return w.logits
+    from wide_bf16_row_gb300 import synth
+
+    vals = synth.bf16_to_float(w.logits)
+    if fmt == "f32":
+        return np.ascontiguousarray(vals).view(np.uint32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return vals.astype(np.float16).view(np.uint16)
+
+
+def run_label(w, fmt: str, k: int) -> str:
+    """The workload's name, with the format and k when they are not its own."""
+    return w.name if (fmt == "bf16" and k == w.k) else f"{w.rows}x{w.cols}_k{k}_{fmt}"
+
+
 def workload_config(w, extra: dict | None = None) -> dict:
     cfg = {"workload": w.name, "rows": w.rows, "cols": w.cols, "k": w.k,
            "row_stride": w.row_stride}
@@ -200,24 +229,27 @@ def workload_config(w, extra: dict | None = None) -> dict:
 
 # ----------------------------------------------------------------------------- oracle timing
 
-def time_oracle(w, budget_s: float, rows_per_call: int | None = None) -> dict:
+def time_oracle(w, budget_s: float, rows_per_call: int | None = None, bits: np.ndarray | None = None,
+                k: int | None = None, fmt: str = "bf16") -> dict:
     """The CPU oracle (as it stands) on a bounded sample of the workload's rows,
     all host cores; repeated until ``budget_s`` of wall time has passed."""
     import oracle
 
     cores = host_cores()
+    bits = w.logits if bits is None else bits
+    k = w.k if k is None else k
     n = min(w.rows, rows_per_call or max(cores, 1))
-    sample = w.logits[:n]
-    oracle.topk(sample, w.cols, w.k, nthreads=cores)  # load + warm
+    sample = bits[:n]
+    oracle.topk(sample, w.cols, k, nthreads=cores, dtype=fmt)  # load + warm
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.topk(sample, w.cols, w.k, nthreads=cores)
+        oracle.topk(sample, w.cols, k, nthreads=cores, dtype=fmt)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
     return {"value": n * reps / el, "unit": "rows/s", "cores": min(cores, n), "kind": "oracle",
-            "sample": f"first {n} rows of {w.name}, {reps} repetitions, {el:.2f} s wall, "
+            "sample": f"first {n} rows of {run_label(w, fmt, k)}, {reps} repetitions, {el:.2f} s wall, "
                       f"{min(cores, n)} threads"}
 
 
@@ -228,18 +260,20 @@ def run_reference(args) -> None:
     import oracle
 
     w = make_workload(args.workload)
+    k = args.k or w.k
+    bits = format_bits(w, args.dtype)
     cores = host_cores()
     # one step = the top-k of one row of the batch; `cores` steps run side by side
     per_call = max(1, cores)
     order = np.arange(args.steps + args.warmup) % w.rows
     for s in range(0, args.warmup, per_call):
         rows = order[s: min(args.warmup, s + per_call)]
-        oracle.topk(w.logits[rows], w.cols, w.k, nthreads=cores)
+        oracle.topk(bits[rows], w.cols, k, nthreads=cores, dtype=args.dtype)
     t0 = time.perf_counter()
     done = 0
     while done < args.steps:
         rows = order[args.warmup + done: args.warmup + min(args.steps, done + per_call)]
-        oracle.topk(w.logits[rows], w.cols, w.k, nthreads=cores)
+        oracle.topk(bits[rows], w.cols, k, nthreads=cores, dtype=args.dtype)
         done += len(rows)
     el = time.perf_counter() - t0
     value = args.steps / el
@@ -248,11 +282,14 @@ def run_reference(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(w, {"step": "top-k of one row; host-core batches of "
-                                              f"{per_call} rows"}),
+        "config": workload_config(w, {
+            **({} if run_label(w, args.dtype, k) == w.name
+               else {"workload": run_label(w, args.dtype, k), "k": k, "format": args.dtype}),
+            "step": f"top-k of one row; host-core batches of {per_call} rows"}),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": min(cores, per_call),
                          "kind": "oracle",
-                         "sample": f"{args.steps} rows of {w.name} (cycling), {per_call} per call"},
+                         "sample": f"{args.steps} rows of {run_label(w, args.dtype, k)} (cycling), "
+                                   f"{per_call} per call"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -276,23 +313,38 @@ def run_ours(args) -> None:
     from wide_bf16_row_gb300 import topk
 
     w = make_workload(args.workload, rank)
-    rows, cols, k, stride = w.rows, w.cols, w.k, w.row_stride
-    in_bytes = rows * stride * 2
+    rows, cols, stride = w.rows, w.cols, w.row_stride
+    k = args.k or w.k
+    fmt = args.dtype
+    code, _ = FORMATS[fmt]
+    bits = format_bits(w, fmt)
+    esize = bits.dtype.itemsize
+    tint = torch.int32 if esize == 4 else torch.int16
+    in_bytes = rows * stride * esize
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     nbuf = max(2, math.ceil(4 * l2 / in_bytes))
-    host = torch.from_numpy(w.logits.view(np.int16))
+    host = torch.from_numpy(bits.view(np.int32 if esize == 4 else np.int16))
     bufs = [host.to(dev) for _ in range(nbuf)]
     views = [b.as_strided((rows, cols), (stride, 1)) for b in bufs]
     out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
-           torch.empty((rows, k), dtype=torch.int16, device=dev),
+           torch.empty((rows, k), dtype=tint, device=dev),
            torch.empty((rows,), dtype=torch.int32, device=dev),
            torch.empty((rows,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
     plan_arg = args.plan
-    plan = plan_arg if plan_arg else topk.plan(rows, cols, k)
+    # bf16 with k <= 64 runs the tf_topk_bf16 plans; anything else the wide kernel
+    fast = fmt == "bf16" and k <= FAST_MAX_K and plan_arg != 64
+    plan = (plan_arg if plan_arg else topk.plan(rows, cols, k)) if fast else 64
+    label = run_label(w, fmt, k)
+
+    def call(view):
+        if fmt == "bf16" and k == w.k and plan_arg != 64:
+            topk.topk_bf16(view, k, plan=plan_arg, out=out, stream=stream)
+        else:
+            topk.select_topk(view, k, dtype=code, plan=plan_arg, out=out, stream=stream)
 
     def step(i: int):
-        topk.topk_bf16(views[i % nbuf], k, plan=plan_arg, out=out, stream=stream)
+        call(views[i % nbuf])
 
     for i in range(args.warmup):
         step(i)
@@ -335,7 +387,7 @@ def run_ours(args) -> None:
     # average launch duration: this rank's timed region over its launches
     avg_launch_s = elapsed_ms / 1e3 / args.steps
     isolated_s = statistics.mean(launch_ms) / 1e3 if launch_ms else None
-    alg_bytes = w.algorithmic_bytes()
+    alg_bytes = rows * cols * esize + rows * k * (4 + esize) + rows * 8
     peak, peak_kind = measured_peak_hbm()
     achieved = alg_bytes / avg_launch_s / 1e9
 
@@ -352,7 +404,7 @@ def run_ours(args) -> None:
     h_out = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out)
     for _ in range(2):
         dbuf.copy_(pinned_in, non_blocking=True)
-        topk.topk_bf16(dview, k, plan=plan_arg, out=out, stream=stream)
+        call(dview)
         for h, d in zip(h_out, out):
             h.copy_(d, non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -362,19 +414,19 @@ def run_ours(args) -> None:
     e0.record(stream)
     for _ in range(e2e_steps):
         dbuf.copy_(pinned_in, non_blocking=True)
-        topk.topk_bf16(dview, k, plan=plan_arg, out=out, stream=stream)
+        call(dview)
         for h, d in zip(h_out, out):
             h.copy_(d, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = whole_job_rate(rows, e2e_steps, world, e2e_ms / 1e3)
-    h2d = rows * stride * 2
-    d2h = rows * k * 4 + rows * k * 2 + rows * 4 + rows * 4
+    h2d = rows * stride * esize
+    d2h = rows * k * 4 + rows * k * esize + rows * 4 + rows * 4
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(w, budget_s=args.cpu_seconds)
+        cpu = time_oracle(w, budget_s=args.cpu_seconds, bits=bits, k=k, fmt=fmt)
 
     if rank == 0:
         line = {
@@ -388,11 +440,11 @@ def run_ours(args) -> None:
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "u16",
+            "dtype": "u32" if esize == 4 else "u16",
             "data": "synthetic",
             "config": workload_config(w, {
-                "plan": {1: "single", 2: "cluster2", 4: "cluster4", 8: "cluster8", 16: "cluster16",
-                         32: "stream"}.get(plan, str(plan)),
+                **({} if label == w.name else {"workload": label, "k": k, "format": fmt}),
+                "plan": PLAN_NAME.get(plan, str(plan)),
                 "l2": f"inputs rotate over {nbuf} device copies ({nbuf * in_bytes / 1e6:.0f} MB, "
                       f"L2 {l2 / 1e6:.0f} MB)",
                 "parallelism": f"replicas x{world} (rows independent, no exchange)"}),
@@ -400,7 +452,7 @@ def run_ours(args) -> None:
             "us_per_call_isolated": isolated_s * 1e6 if isolated_s else None,
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(plan, w.name),
+                         "frac": achieved / peak, "traffic": profiled_traffic(plan, label),
                          "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "launches_timed": args.steps,
@@ -424,7 +476,10 @@ def main(argv=None) -> None:
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--plan", type=int, default=0,
-                    help="TF_TOPK_PLAN_* code: 0 auto, 1 single, 2/4/8/16 cluster, 32 stream")
+                    help="TF_TOPK_PLAN_* code: 0 auto, 1 single, 2/4/8/16 cluster, 32 stream, 64 wide")
+    ap.add_argument("--dtype", choices=sorted(FORMATS), default="bf16",
+                    help="logit format (tf_topk_select for f16 / f32)")
+    ap.add_argument("--k", type=int, default=None, help="k (default: the workload's)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -948,6 +948,18 @@ __device__ __forceinline__ void grid_dependency_wait()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The wait alone; a kernel using it lets its dependents be scheduled only
+// once each of its CTAs reaches grid_dependents_go, near its end.
+__device__ __forceinline__ void grid_dependency_wait_only()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependents_go()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Stream-plan ranges.  CTA b nominally starts at vector b * per of the
 // rows x vectors space; the start is moved to the nearest multiple of kThreads
 // vectors from its row's start, or to the row's end when less than kThreads
@@ -1860,7 +1872,9 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
     const T *row = logits + r * row_stride;
-    grid_dependency_wait();
+    // one CTA per row: the next launch is placed as this one's CTAs finish
+    // (scheduled early, its CTAs would crowd the SMs still running rows)
+    grid_dependency_wait_only();
     if (tid == 0) {
         sm.n_ent = 0;
         sm.flags = 0;
@@ -2037,6 +2051,7 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     }
 
     // ---- the row: the first cnt entries, original bits re-read by column
+    grid_dependents_go();
     for (int i = tid; i < k; i += kWideThreads) {
         if (i < cnt) {
             const int32_t c = (int32_t)(~(uint32_t)res[i]);
