@@ -332,9 +332,13 @@ def run_ours(args) -> None:
            torch.empty((rows,), dtype=torch.int32, device=dev))
     stream = torch.cuda.current_stream(dev)
     plan_arg = args.plan
-    # bf16 with k <= 64 runs the tf_topk_bf16 plans; anything else the wide kernel
-    fast = fmt == "bf16" and k <= FAST_MAX_K and plan_arg != 64
+    # bf16 with k <= 64 runs the tf_topk_bf16 plans, fp16 with k <= 64 their
+    # cluster plans (one CTA per row becomes the wide kernel); anything else
+    # the wide kernel
+    fast = fmt in ("bf16", "f16") and k <= FAST_MAX_K and plan_arg != 64
     plan = (plan_arg if plan_arg else topk.plan(rows, cols, k)) if fast else 64
+    if fmt == "f16" and plan in (1, 32):
+        plan = 64
     label = run_label(w, fmt, k)
 
     def call(view):

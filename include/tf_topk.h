@@ -269,10 +269,12 @@ int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows
  *                `dtype` (the original bits); out_count int32 [rows];
  *                out_nonfinite_mask uint32 [rows] (1 NaN, 2 +inf, 4 -inf).
  * bf16 with k <= TF_TOPK_MAX_K runs the plans of tf_topk_bf16 (the same
- * results, byte for byte); everything else runs the wide kernel: one CTA per
- * row, two passes over the row (a bound from each thread's four best keys,
- * then every element reaching it, sorted), with an exact counting search
- * when ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
+ * results, byte for byte).  fp16 with k <= TF_TOPK_MAX_K runs the cluster
+ * plans (it shares bf16's order-preserving key map; only its special values
+ * differ), except where AUTO would give a row one CTA.  Everything else runs
+ * the wide kernel: one CTA per row, two passes over the row (a bound from
+ * each thread's best keys, then every element reaching it, ranked), with an
+ * exact counting search when ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
  * Returns a TF_TOPK_* status: ERR_DTYPE for an unknown format, ERR_K,
  * ERR_SHAPE, ERR_NULL, ERR_ALIGN as for tf_topk_bf16.
  */
@@ -285,9 +287,9 @@ int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows
 int tf_topk_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
                    int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream);
 
-/* tf_topk_select with a plan: TF_TOPK_PLAN_AUTO, TF_TOPK_PLAN_WIDE, or (bf16
- * with k <= TF_TOPK_MAX_K only) a plan of tf_topk_bf16_with_plan; anything
- * else returns TF_TOPK_ERR_PLAN. */
+/* tf_topk_select with a plan: TF_TOPK_PLAN_AUTO, TF_TOPK_PLAN_WIDE, or, with
+ * k <= TF_TOPK_MAX_K, a plan of tf_topk_bf16_with_plan (bf16) or a cluster
+ * plan CLUSTER2..16 (fp16); anything else returns TF_TOPK_ERR_PLAN. */
 int tf_topk_select_with_plan(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride,
                              int32_t k, int32_t *out_idx, void *out_val, int32_t *out_count,
                              uint32_t *out_nonfinite_mask, int32_t plan, void *stream);

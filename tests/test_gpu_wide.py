@@ -7,8 +7,10 @@ Cases: every format over k from 1 to 1024; padded strides and row bases off
 the 16-byte grid (the unaligned head and tail); rows shorter than k; the
 heavy-tie fallback (all +-0, few distinct values, a k-th key shared by
 thousands of columns); all-NaN rows; fp32 near-ties in the low half; the
-256 x 248320 bench shape forced through the wide kernel; and bf16 with
-k <= 64 through tf_topk_select against tf_topk_bf16."""
+256 x 248320 bench shape forced through the wide kernel; bf16 with k <= 64
+through tf_topk_select against tf_topk_bf16; and fp16 with k <= 64 on the
+cluster plans it shares with bf16 (the same key map, fp16's special
+values)."""
 from __future__ import annotations
 
 import numpy as np
@@ -151,3 +153,34 @@ def test_bf16_small_k_matches_tf_topk_bf16():
     for plan in (0, 2, 8):
         got = gpu_select(w.logits, w.cols, w.k, "bf16", plan=plan)
         assert_same(got, gpu_topk(w.logits, w.cols, w.k, plan=plan), f"select plan {plan}")
+
+
+@pytest.mark.parametrize("plan", [0, 2, 4, 8, 16])
+def test_f16_on_the_cluster_plans(plan):
+    """fp16, k <= 64, on CLUSTER2..16 (and AUTO): mixed rows with every fp16
+    special, padded strides, an unaligned row base, heavy ties (the exact
+    path) and all-NaN rows, against the oracle."""
+    x = gen("f16", 6, 70001, 3 + plan, 70016, special_frac=0.02, dup_frac=0.05)
+    for k in (1, 20, 64):
+        assert_same(gpu_select(x, 70001, k, "f16", plan=plan), oracle.topk(x, 70001, k, dtype="f16"),
+                    f"f16 plan {plan} k{k}")
+    assert_same(gpu_select(x, 70001, 33, "f16", plan=plan, offset=3), oracle.topk(x, 70001, 33, dtype="f16"),
+                f"f16 plan {plan} offset 3")
+    rng = np.random.default_rng(plan)
+    ties = np.zeros((5, 40000), np.uint16)
+    ties[0] = rng.integers(0, 2, size=40000).astype(np.uint16) << np.uint16(15)      # +-0
+    ties[1] = rng.choice(np.array([0x3C00, 0x4000, 0xBC00], np.uint16), size=40000)  # three values
+    ties[2] = 0x7E00                                                                 # all NaN
+    ties[3] = rng.choice(np.array([0x7C00, 0xFC00, 0x0001, 0x8001], np.uint16), size=40000)  # infs, subnormals
+    ties[4] = (rng.standard_normal(40000) * 2).astype(np.float16).view(np.uint16)
+    for k in (1, 64):
+        assert_same(gpu_select(ties, 40000, k, "f16", plan=plan), oracle.topk(ties, 40000, k, dtype="f16"),
+                    f"f16 ties plan {plan} k{k}")
+
+
+def test_f16_bench_shape_auto():
+    """256 x 248320 fp16 (the bench workload's values rounded to fp16), AUTO plan."""
+    w = synth.config_draft_window()
+    with np.errstate(over="ignore"):
+        x = synth.bf16_to_float(w.logits).astype(np.float16).view(np.uint16)
+    assert_same(gpu_select(x, w.cols, w.k, "f16"), oracle.topk(x, w.cols, w.k, dtype="f16"), "f16 256x248320")

@@ -106,9 +106,25 @@ static_assert(kStages >= 2, "a ring needs two stages");
 static_assert(kMinVecsPerCta >= 4 * kThreads, "moved range starts stay strictly increasing");
 static_assert(kVecPerThread * 4 == 32, "the candidate scan maps a lane to one word of a thread's slice");
 
-constexpr uint32_t kEmptyVal = 0x7FC0;
-constexpr uint32_t kKeyPosInf = 0xFF80;
-constexpr uint32_t kKeyNegInf = 0x007F;
+// What the fast kernels need to know of a 16-bit format; the order-preserving
+// key map (sign-magnitude flip) is the same for every IEEE 16-bit format.
+// Keys above the +inf key or below the -inf key are NaN; empty output slots
+// hold the format's quiet NaN.
+template <int kFmt>
+struct Fmt16;
+template <>
+struct Fmt16<TF_TOPK_DTYPE_BF16> {
+    static constexpr uint32_t kKeyPosInf = 0xFF80, kKeyNegInf = 0x007F;
+    static constexpr uint32_t kRawPosInf = 0x7F80, kRawNegInf = 0xFF80, kEmpty = 0x7FC0;
+};
+template <>
+struct Fmt16<TF_TOPK_DTYPE_F16> {
+    static constexpr uint32_t kKeyPosInf = 0xFC00, kKeyNegInf = 0x03FF;
+    static constexpr uint32_t kRawPosInf = 0x7C00, kRawNegInf = 0xFC00, kEmpty = 0x7E00;
+};
+constexpr int kBf16 = TF_TOPK_DTYPE_BF16;
+
+constexpr uint32_t kEmptyVal = Fmt16<kBf16>::kEmpty;
 constexpr uint32_t kKeyNegZero = 0x7FFF;
 constexpr uint32_t kKeyPosZero = 0x8000;
 
@@ -276,6 +292,7 @@ __device__ __forceinline__ uint32_t count_at_least(const uint32_t *keys, uint32_
 // keys have been staged in `keys` in column order (0 = not a candidate).
 // Writes exactly k candidates -- the chunk's top-k within that set -- into
 // sm.cand.  Block-uniform; every thread calls it.
+template <int kFmt = kBf16>
 __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor, int k, SmemCore &sm)
 {
     const int tid = threadIdx.x;
@@ -301,7 +318,7 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
     }
     const uint32_t kstar = lo;
     const uint32_t above =
-        (kstar >= kKeyPosInf) ? 0u : block_sum(count_at_least(keys, kstar + 1), sm, parity);
+        (kstar >= Fmt16<kFmt>::kKeyPosInf) ? 0u : block_sum(count_at_least(keys, kstar + 1), sm, parity);
     const uint32_t need = (uint32_t)k - above; // ties at K* to take, lowest columns first
 
     // 2. Each thread owns a contiguous run of columns; an exclusive scan of the
@@ -385,6 +402,7 @@ __device__ __noinline__ uint4 load_edge_vector(const uint16_t *rowp, int32_t col
 // (vector i at stage[i * kThreads + tid]); columns outside the row and NaNs
 // become key 0 and the row's non-finite flags are recorded.  Returns the
 // thread's max key over what remains.
+template <int kFmt = kBf16>
 __device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_t cols, int nvalid,
                                           SmemCore &sm)
 {
@@ -402,12 +420,12 @@ __device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_
                 uint32_t key = (qw[w] >> (16 * h)) & 0xFFFFu;
                 if (c < 0 || c >= cols) {
                     key = 0;
-                } else if (key > kKeyPosInf || key < kKeyNegInf) {
+                } else if (key > Fmt16<kFmt>::kKeyPosInf || key < Fmt16<kFmt>::kKeyNegInf) {
                     flags |= 1u; // NaN
                     key = 0;
-                } else if (key == kKeyPosInf) {
+                } else if (key == Fmt16<kFmt>::kKeyPosInf) {
                     flags |= 2u;
-                } else if (key == kKeyNegInf) {
+                } else if (key == Fmt16<kFmt>::kKeyNegInf) {
                     flags |= 4u;
                 }
                 tmax = max(tmax, key);
@@ -427,7 +445,7 @@ __device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_
 // thread's max key is returned.  kFull: every vector of the chunk lies wholly
 // inside the row (no predicates).  `stage` is the chunk's 32 KB of shared
 // memory, this thread's slots of which the rare exact pass may use.
-template <bool kFull>
+template <bool kFull, int kFmt = kBf16>
 __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4], int nvalid,
                                                int32_t col_base, int32_t cols, uint4 *stage, SmemCore &sm)
 {
@@ -449,11 +467,11 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
     const uint32_t tmin = min(mn & 0xFFFFu, mn >> 16);
 
     // ---- exact key pass (columns outside the row, NaN, +-inf), through shared memory
-    if (tmax >= kKeyPosInf || tmin <= kKeyNegInf) {
+    if (tmax >= Fmt16<kFmt>::kKeyPosInf || tmin <= Fmt16<kFmt>::kKeyNegInf) {
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i)
             stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
-        tmax = fix_keys(stage, col_base, cols, nvalid, sm);
+        tmax = fix_keys<kFmt>(stage, col_base, cols, nvalid, sm);
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i) {
             const uint4 q = stage[i * kThreads + tid];
@@ -475,6 +493,7 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
 // also shows a +inf/+NaN (>= 0x7F80) and the unsigned max a -inf/-NaN
 // (>= 0xFF80).  Returns false -- the keys are needed -- when the thread holds
 // any of those or no non-negative value at all.
+template <int kFmt = kBf16>
 __device__ __forceinline__ bool raw_tmax(const uint32_t (&kv)[kVecPerThread][4], uint32_t &tmax)
 {
     uint32_t smx = 0x80008000u, umx = 0;
@@ -487,7 +506,7 @@ __device__ __forceinline__ bool raw_tmax(const uint32_t (&kv)[kVecPerThread][4],
         }
     const int32_t smax = max((int32_t)(int16_t)(smx & 0xFFFFu), (int32_t)(int16_t)(smx >> 16));
     const uint32_t umax = max(umx & 0xFFFFu, umx >> 16);
-    if (smax < 0 || smax >= (int32_t)0x7F80 || umax >= 0xFF80u) return false;
+    if (smax < 0 || smax >= (int32_t)Fmt16<kFmt>::kRawPosInf || umax >= Fmt16<kFmt>::kRawNegInf) return false;
     tmax = (uint32_t)smax + 0x8000u;
     return true;
 }
@@ -567,6 +586,7 @@ __device__ __forceinline__ bool spill_hits(uint32_t (&kv)[kVecPerThread][4], uin
 // `stage` (0 elsewhere), re-read from global memory (the registers that held
 // the chunk already carry the next one).  Keys are exact as in fix_keys:
 // columns outside the row and NaN become 0.
+template <int kFmt = kBf16>
 __device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, ChunkGeom geo, int32_t cbeg,
                                            int nvalid, int32_t col_base, uint32_t t_floor)
 {
@@ -585,7 +605,9 @@ __device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, Chu
                 for (int h = 0; h < 2; ++h) {
                     const int32_t c = col_base + lv * 8 + 2 * w + h;
                     uint32_t key = (key2 >> (16 * h)) & 0xFFFFu;
-                    if (c < 0 || c >= geo.cols || key > kKeyPosInf || key < kKeyNegInf || key < t_floor) key = 0;
+                    if (c < 0 || c >= geo.cols || key > Fmt16<kFmt>::kKeyPosInf || key < Fmt16<kFmt>::kKeyNegInf ||
+                        key < t_floor)
+                        key = 0;
                     out |= key << (16 * h);
                 }
                 qw[w] = out;
@@ -601,6 +623,7 @@ __device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, Chu
 // above kCandCap (heavy ties) the chunk is restaged and selected exactly, and
 // n = k.  `base` (block-uniform) is the candidate counter's value before the
 // chunk and after it.  Block-uniform.
+template <int kFmt = kBf16>
 __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, int k, SmemCore &sm, uint4 *stage,
                                                     const uint4 *vbase, const ChunkGeom &geo, int32_t cbeg,
                                                     int nvalid, int32_t col_base, uint32_t &base)
@@ -620,9 +643,9 @@ __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, 
     uint32_t n = total - base;
     base = total;
     if (n > (uint32_t)kCandCap) {
-        restage_chunk(stage, vbase, geo, cbeg, nvalid, col_base, t_floor);
+        restage_chunk<kFmt>(stage, vbase, geo, cbeg, nvalid, col_base, t_floor);
         __syncthreads();
-        exact_select(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm); // counts from 0
+        exact_select<kFmt>(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm); // counts from 0
         n = sm.n_cand; // == k
         base = n;
     }
@@ -867,6 +890,7 @@ __device__ __forceinline__ const uint64_t *merge_tree(SmemGather &sm, int nl, in
     return src[0];
 }
 
+template <int kFmt = kBf16>
 __device__ __forceinline__ void write_row(int64_t row, const uint64_t *list, int len, uint32_t flags,
                                           int k, int32_t *out_idx, uint16_t *out_val,
                                           int32_t *out_count, uint32_t *out_mask)
@@ -879,7 +903,7 @@ __device__ __forceinline__ void write_row(int64_t row, const uint64_t *list, int
             out_val[o] = (uint16_t)(e & 0xFFFFu);
         } else {
             out_idx[o] = -1;
-            out_val[o] = (uint16_t)kEmptyVal;
+            out_val[o] = (uint16_t)Fmt16<kFmt>::kEmpty;
         }
     }
     if (threadIdx.x == 0) {
@@ -1353,7 +1377,7 @@ __device__ __forceinline__ void load_chunk(uint32_t (&kv)[kVecPerThread][4], con
 
 // grid.x = rows * S; the launch groups each row's S CTAs into one cluster
 // (cluster rank == span).
-template <int S>
+template <int S, int kFmt = kBf16>
 __global__ void __launch_bounds__(kThreads, 4)
 topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
                     int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
@@ -1393,11 +1417,11 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         const bool full = nvalid == kChunkVecs && cbeg >= geo.vfull0 && cend <= geo.vfull1;
         // a full chunk inside the row: the max from the raw bits where it can be
         uint32_t tmax = 0;
-        const bool raw = full && raw_tmax(kv, tmax);
+        const bool raw = full && raw_tmax<kFmt>(kv, tmax);
         if (!raw) {
             geo.cbeg = cbeg;
             geo.cend = cend;
-            tmax = chunk_keys<false>(kv, nvalid, col_base, cols, keys, sm);
+            tmax = chunk_keys<false, kFmt>(kv, nvalid, col_base, cols, keys, sm);
         }
         const uint32_t t_floor = chunk_floor(tmax, nvalid, k, sm, run_i, run_len);
         const bool hit = spill_hits(kv, tmax, raw, t_floor, keys);
@@ -1405,7 +1429,8 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         // the candidate scan, the rank and the merge
         const bool more = cend < v_end;
         if (more) load_chunk(kv, vbase, geo, cend, v_end, cols);
-        const uint32_t n = push_candidates(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base, cand_base);
+        const uint32_t n =
+            push_candidates<kFmt>(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base, cand_base);
         if (n > (uint32_t)kCandCap && more) load_chunk(kv, vbase, geo, cend, v_end, cols); // reissued after the exact path
         if (n) merge_candidates(n, col_base, k, sm, run_i, free_i, run_len);
         __syncthreads(); // the merge is complete before the next chunk reads its bound
@@ -1431,7 +1456,7 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     for (int s = 0; s < S; ++s) flags |= sg.gflags[s];
     int flen = 0;
     const uint64_t *fin = merge_tree(sg, S, k, flen);
-    write_row(row, fin, flen, flags, k, out_idx, out_val, out_count, out_mask);
+    write_row<kFmt>(row, fin, flen, flags, k, out_idx, out_val, out_count, out_mask);
 }
 
 // ---------------------------------------------------------------- shard-list merge kernel
@@ -2109,7 +2134,10 @@ int device_setup(int *dev_out, int *sm_count)
         if (major != 10 || minor != 3) {
             d.status = TF_TOPK_ERR_DEVICE;
         } else {
-            e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            e = cudaFuncSetAttribute(topk_cluster_kernel<16, kBf16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(topk_cluster_kernel<16, TF_TOPK_DTYPE_F16>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kStreamSmemBytes);
@@ -2239,7 +2267,7 @@ int32_t pick_plan(int64_t rows, int64_t cols, int32_t k, int sm_count)
     return s;
 }
 
-template <int S>
+template <int S, int kFmt = kBf16>
 cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, int64_t row_stride, int32_t k,
                            int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_mask,
                            cudaStream_t stream)
@@ -2261,7 +2289,7 @@ cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, i
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<S>, logits + r0 * row_stride, cols,
+        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<S, kFmt>, logits + r0 * row_stride, cols,
                                            row_stride, k, out_idx + r0 * k, out_val + r0 * k,
                                            out_count + r0, out_mask + r0);
         if (e != cudaSuccess) return e;
@@ -2534,9 +2562,11 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
     if (k < 1 || k > kWideMaxK) return TF_TOPK_ERR_K;
     if (rows < 0 || cols < 1 || row_stride < cols || cols > (int64_t)INT32_MAX - 64) return TF_TOPK_ERR_SHAPE;
     if (rows > 0 && row_stride > INT64_MAX / rows) return TF_TOPK_ERR_SHAPE;
+    const bool cluster_plan = plan == TF_TOPK_PLAN_CLUSTER2 || plan == TF_TOPK_PLAN_CLUSTER4 ||
+                              plan == TF_TOPK_PLAN_CLUSTER8 || plan == TF_TOPK_PLAN_CLUSTER16;
     if (plan != TF_TOPK_PLAN_AUTO && plan != TF_TOPK_PLAN_WIDE &&
-        (dtype != TF_TOPK_DTYPE_BF16 || k > kMaxK))
-        return TF_TOPK_ERR_PLAN; // the fast plans take bf16 with k <= 64 only
+        !(k <= kMaxK && (dtype == TF_TOPK_DTYPE_BF16 || (dtype == TF_TOPK_DTYPE_F16 && cluster_plan))))
+        return TF_TOPK_ERR_PLAN; // bf16: every plan; fp16: the cluster plans; both with k <= 64
     if (rows == 0) return TF_TOPK_OK;
     if (!logits || !out_idx || !out_val || !out_count || !out_mask) return TF_TOPK_ERR_NULL;
     const uintptr_t esz = dtype == TF_TOPK_DTYPE_F32 ? 4 : 2;
@@ -2551,6 +2581,37 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
     const int st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == TF_TOPK_DTYPE_F16 && k <= kMaxK && plan != TF_TOPK_PLAN_WIDE) {
+        // fp16 shares bf16's key map: the cluster plans, with fp16's special values
+        int p = plan == TF_TOPK_PLAN_AUTO ? pick_plan(rows, cols, k, sm_count) : plan;
+        const uint16_t *x = static_cast<const uint16_t *>(logits);
+        uint16_t *ov = static_cast<uint16_t *>(out_val);
+        const int32_t c = (int32_t)cols;
+        cudaError_t e = cudaSuccess;
+        switch (p) {
+        case TF_TOPK_PLAN_CLUSTER2:
+            e = launch_cluster<2, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            break;
+        case TF_TOPK_PLAN_CLUSTER4:
+            e = launch_cluster<4, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            break;
+        case TF_TOPK_PLAN_CLUSTER8:
+            e = launch_cluster<8, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            break;
+        case TF_TOPK_PLAN_CLUSTER16:
+            e = launch_cluster<16, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask,
+                                                      s);
+            break;
+        default: // narrow rows, where AUTO would take one CTA per row: the wide kernel
+            p = TF_TOPK_PLAN_WIDE;
+            break;
+        }
+        if (p != TF_TOPK_PLAN_WIDE) {
+            if (e == cudaSuccess) e = cudaGetLastError();
+            if (e != cudaSuccess) return fail_cuda(e);
+            return TF_TOPK_OK;
+        }
+    }
     const bool small = k <= kWideSmallK;
     switch (dtype) {
     case TF_TOPK_DTYPE_BF16:
