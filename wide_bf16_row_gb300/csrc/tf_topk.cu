@@ -1656,7 +1656,7 @@ topk_nucleus_kernel(const uint16_t *__restrict__ val, const int32_t *__restrict_
 // are collected, and the ties at K* are taken in column order from
 // contiguous per-thread column ranges.
 
-constexpr int kWideThreads = 256;
+constexpr int kWideThreads = 512;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideUnroll = 8;                  // 16-byte loads in flight per thread
 constexpr int kWideCap = 4096;                  // entries pass 2 may collect
@@ -1886,7 +1886,7 @@ __device__ __forceinline__ uint32_t warp_jth(uint32_t (&t)[Q], uint32_t j)
 }
 
 template <typename T, int kFmt, int Q>
-__global__ void __launch_bounds__(kWideThreads)
+__global__ void __launch_bounds__(kWideThreads, 2)
 topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
                  int32_t *__restrict__ out_idx, T *__restrict__ out_val, int32_t *__restrict__ out_count,
                  uint32_t *__restrict__ out_mask)
