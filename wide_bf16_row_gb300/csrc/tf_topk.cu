@@ -9,40 +9,48 @@
 // strides).  The conventions the pages leave open are stated in
 // include/tf_topk.h.
 //
-// Common machinery (both kernels):
+// Common machinery of the two bf16 / fp16 kernels (for k <= 64):
 //   * A CTA processes a row a chunk at a time: kThreads x kVecPerThread
 //     16-byte vectors (16384 columns), held in registers as order-preserving
 //     16-bit keys, two per register: positive bits b -> b | 0x8000, negative
 //     bits b -> ~b.  -0 and +0 land on the neighbouring keys 0x7FFF / 0x8000 and
 //     are treated as one score wherever a threshold or a comparison is taken.
+//     The key map is the same for fp16; only the special values differ
+//     (Fmt16<format>).
 //   * Prefilter: every thread keeps the max key of its elements; each warp finds
 //     the j-th largest of its 32 thread maxima (j = ceil(k / warps)); the
 //     minimum T over warps is reached by at least k elements, so the chunk's
-//     top-k lies in {key >= T}.  Only those candidates (typically a few times k
-//     out of 16384) touch shared memory.
+//     top-k lies in {key >= T}.  Once a running list holds k entries, its k-th
+//     key is the bound instead.  Only candidates touch shared memory.
 //   * Candidates are ranked exactly with a unique 32-bit composite
 //     (key << 16 | ~chunk-local column).  Chunks with heavy ties (e.g. an
 //     all-zero row) overflow the candidate buffer and take an exact path: a
 //     binary search for the k-th key, then the lowest columns among the ties at
 //     that key, ranked by a block scan in column order.
 //   * A running list (<= k entries, 64-bit: key | ~column | original bits)
-//     absorbs the chunks of a row piece; pieces are merged pairwise (the
-//     pages' tournament) in the same order.
+//     absorbs the chunks of a row piece; pieces are merged (the pages'
+//     tournament) in the same order.
 //
-// Kernel 1, topk_stream_kernel (the default plan): a persistent grid of
+// topk_cluster_kernel<S, format> (the plans tf_topk_bf16 picks): S CTAs of a
+// thread-block cluster split one row into S spans, load with 16-byte register
+// loads, and merge through distributed shared memory in the leader CTA.  Each
+// chunk's loads are issued as soon as the previous chunk's candidates are
+// spilled, and candidates are ranked and merged into the running list in one
+// phase.
+//
+// topk_stream_kernel (plans SINGLE and STREAM): a persistent grid of
 // kStreamCtasPerSm CTAs per SM.  The rows x vectors space is cut into equal
-// contiguous ranges, one per CTA, so every SM gets the same number of bytes
-// whatever the shape.  Each CTA streams its range through a kStages-deep
-// shared-memory ring filled by TMA bulk copies (cp.async.bulk + mbarrier): the
-// next chunk is in flight while one is selected.  A row cut by a range boundary leaves one partial list per
-// piece in a small scratch area; the last CTA to finish a piece of that row
-// (an atomic ticket) merges them and writes the row.  With one range per row
-// the same kernel is the single-CTA control path.
+// contiguous ranges, one per CTA.  Each CTA streams its range through a
+// kStages-deep shared-memory ring filled by TMA bulk copies (cp.async.bulk +
+// mbarrier).  A row cut by a range boundary leaves one partial list per piece
+// in a small scratch area; the last CTA to finish a piece of that row (an
+// atomic ticket) merges them and writes the row.  With one range per row the
+// same kernel is the single-CTA control path.
 //
-// Kernel 2, topk_cluster_kernel<S>: S CTAs of a thread-block cluster split one
-// row into S spans, load with 16-byte register loads, and merge through
-// distributed shared memory in the leader CTA.  Kept as a measured
-// alternative plan.
+// Also here: topk_merge_kernel (per-shard lists into each row's top k),
+// topk_nucleus_kernel (top-p probabilities over the lists) and
+// topk_wide_kernel (bf16 / fp16 / fp32 rows, k up to 1024: a bound from each
+// thread's best keys, then every element reaching it, ranked).
 //
 // No wait is unbounded: mbarrier waits give up after kWaitLimit polls, record
 // a fault code in a device word, drain their own copies (again bounded) and
