@@ -1824,8 +1824,9 @@ __device__ __forceinline__ void bitonic_desc(K *s, int n)
 {
     for (int size = 2; size <= n; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int sh = __ffs(stride) - 1; // stride is a power of two
             for (int i = threadIdx.x; i < (n >> 1); i += kWideThreads) {
-                const int lo = 2 * stride * (i / stride) + (i % stride), hi = lo + stride;
+                const int lo = ((i >> sh) << (sh + 1)) | (i & (stride - 1)), hi = lo + stride;
                 const bool desc = (lo & size) == 0;
                 const K x = s[lo], y = s[hi];
                 if ((x < y) == desc) {
