@@ -1,8 +1,14 @@
 """Python binding over ``libtf_topk.so`` (C ABI in ``include/tf_topk.h``).
 
-Argument marshalling only: every step of the top-k runs in the library's CUDA
-kernels.  PyTorch supplies device memory and the current stream.  If the
-library has not been built, every entry point raises -- there is no fallback.
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  If the library has
+not been built, every entry point raises -- there is no fallback.
+
+Tensor-level calls: ``topk_bf16`` (bf16 rows, k <= 64, any launch plan),
+``select_topk`` (bf16 / fp16 / fp32 rows, k <= 1024), ``merge_bf16``
+(per-shard lists into each row's top k) and ``nucleus_bf16`` (top-p
+probabilities over the lists).  The raw C entry points are exposed under
+their C names.
 """
 from __future__ import annotations
 
