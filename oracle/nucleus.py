@@ -85,16 +85,29 @@ def nucleus_row(vals: list[float], temperature: float, top_p: float,
     return p, keep, out
 
 
-def nucleus(val_bits: np.ndarray, count: np.ndarray, temperature: float, top_p: float):
+def values_of(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    """Bit patterns of bf16, fp16 or fp32 values -> float64 (exact)."""
+    b = np.asarray(bits)
+    with np.errstate(invalid="ignore"):
+        if dtype == "f16":
+            return b.astype(np.uint16).view(np.float16).astype(np.float64)
+        if dtype == "f32":
+            return b.astype(np.uint32).view(np.float32).astype(np.float64)
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def nucleus(val_bits: np.ndarray, count: np.ndarray, temperature: float, top_p: float, dtype: str = "bf16"):
     """Rows of top-k results -> (prob float64 [rows][k], keep int [rows], and
-    the pre-truncation softmax float64 [rows][k])."""
+    the pre-truncation softmax float64 [rows][k]).  ``val_bits`` holds bit
+    patterns of ``dtype`` ("bf16", "f16" or "f32")."""
     rows, k = val_bits.shape
+    values = values_of(val_bits, dtype)
     prob = np.zeros((rows, k))
     soft = np.zeros((rows, k))
     keep = np.zeros(rows, dtype=np.int64)
     for r in range(rows):
         n = max(0, min(k, int(count[r])))     # a list holds at most k entries
-        vals = [bf16_value(b) for b in val_bits[r, :n]]
+        vals = [float(v) for v in values[r, :n]]
         p, m, out = nucleus_row(vals, temperature, top_p)
         soft[r, :n] = p
         prob[r, :n] = out

@@ -100,3 +100,17 @@ def test_a_fixed_keep_replaces_the_cut():
         vals = [2.5, 1.0, 0.25, -3.0]
         ref = nucleus_row(vals, 0.7, top_p)
         assert nucleus_row(vals, 0.7, 0.5, keep=ref[1]) == ref
+
+
+def test_other_formats_decode_exactly():
+    """fp16 and fp32 lists: the same steps on exactly decoded values."""
+    from oracle.nucleus import values_of
+    assert values_of(np.array([0x3C00, 0x0001, 0xFC00], np.uint16), "f16").tolist() == [1.0, 2.0 ** -24, -math.inf]
+    assert values_of(np.array([0x3F800001], np.uint32), "f32")[0] == 1.0 + 2.0 ** -23
+    assert values_of(np.array([0x4040], np.uint16))[0] == 3.0
+    f32 = np.array([[0x40400000, 0x3F800000, 0]], np.uint32)        # 3, 1
+    prob, keep, soft = nucleus(f32, np.array([2]), 1.0, 0.99, dtype="f32")
+    assert soft[0, 0] == pytest.approx(1 / (1 + math.exp(-2.0))) and keep.tolist() == [2]
+    f16 = np.array([[0x3C00, 0x3C00, 0x3C00, 0x7E00]], np.uint16)    # 1, 1, 1, NaN
+    prob, keep, soft = nucleus(f16, np.array([4]), 0.7, 0.5, dtype="f16")
+    assert keep.tolist() == [2] and soft[0].tolist() == pytest.approx([1 / 3, 1 / 3, 1 / 3, 0.0])
