@@ -295,6 +295,16 @@ int tf_topk_select_with_plan(const void *logits, int32_t dtype, int64_t rows, in
                              uint32_t *out_nonfinite_mask, int32_t plan, void *stream);
 int32_t tf_topk_select_max_k(void); /* == TF_TOPK_MAX_K_WIDE */
 
+/*
+ * tf_topk_nucleus_bf16 for lists of any format tf_topk_select writes: `val`
+ * holds [rows][k] elements of `dtype` (TF_TOPK_DTYPE_*; bf16 and fp16 2-byte
+ * aligned, fp32 4-byte aligned), decoded exactly to float.  Everything else as
+ * tf_topk_nucleus_bf16 (k <= TF_TOPK_MAX_K).  Returns TF_TOPK_ERR_DTYPE for an
+ * unknown format, otherwise the statuses of tf_topk_nucleus_bf16.
+ */
+int tf_topk_nucleus(const void *val, int32_t dtype, const int32_t *count, int64_t rows, int32_t k, float temperature,
+                    float top_p, float *out_prob, int32_t *out_keep, void *stream);
+
 /* Human-readable text for a TF_TOPK_* status (static storage). */
 const char *tf_topk_strerror(int status);
 

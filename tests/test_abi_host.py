@@ -202,3 +202,12 @@ def test_select_zero_rows_and_constants(lib):
     assert (macros["TF_TOPK_DTYPE_BF16"], macros["TF_TOPK_DTYPE_F16"], macros["TF_TOPK_DTYPE_F32"]) == \
         (topk.DTYPE_BF16, topk.DTYPE_F16, topk.DTYPE_F32)
     assert macros["TF_TOPK_PLAN_WIDE"] == topk.PLAN_WIDE and macros["TF_TOPK_ERR_DTYPE"] == topk.ERR_DTYPE
+
+
+def test_nucleus_any_format_guards(lib):
+    from wide_bf16_row_gb300 import topk
+    call = lambda **kw: topk.tf_topk_nucleus(kw.get("val", FAKE), kw.get("dtype", 2), FAKE, kw.get("rows", 4),
+                                             kw.get("k", 8), 0.7, 0.95, FAKE, FAKE, None)
+    assert call(dtype=3) == topk.ERR_DTYPE and call(dtype=-1) == topk.ERR_DTYPE
+    assert call(val=FAKE + 2) == topk.ERR_ALIGN and call(dtype=1, val=FAKE + 1) == topk.ERR_ALIGN
+    assert call(k=65) == topk.ERR_K and call(rows=0) == topk.OK

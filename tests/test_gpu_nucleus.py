@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle.nucleus import bf16_value, nucleus, nucleus_row
+from oracle.nucleus import nucleus, nucleus_row, values_of
 from wide_bf16_row_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -31,27 +31,34 @@ def _lib():
     build.build()
 
 
-def _gpu(val: np.ndarray, count: np.ndarray, temperature: float, top_p: float):
+CODES = {"bf16": 0, "f16": 1, "f32": 2}
+
+
+def _gpu(val: np.ndarray, count: np.ndarray, temperature: float, top_p: float, dtype: str = "bf16"):
     import torch
 
     from wide_bf16_row_gb300 import topk
 
-    v = torch.from_numpy(np.ascontiguousarray(val).view(np.int16)).cuda()
+    sint = np.int32 if dtype == "f32" else np.int16
+    v = torch.from_numpy(np.ascontiguousarray(val).view(sint)).cuda()
     c = torch.from_numpy(np.ascontiguousarray(count, dtype=np.int32)).cuda()
-    prob, keep = topk.nucleus_bf16(v, c, temperature, top_p)
+    if dtype == "bf16":
+        prob, keep = topk.nucleus_bf16(v, c, temperature, top_p)
+    else:
+        prob, keep = topk.nucleus(v, c, temperature, top_p, dtype=CODES[dtype])
     torch.cuda.synchronize()
     return prob.cpu().numpy(), keep.cpu().numpy()
 
 
-def _check(val: np.ndarray, count: np.ndarray, temperature: float, top_p: float, what: str):
-    prob, keep = _gpu(val, count, temperature, top_p)
-    _compare(prob, keep, val, count, temperature, top_p, what)
+def _check(val: np.ndarray, count: np.ndarray, temperature: float, top_p: float, what: str, dtype: str = "bf16"):
+    prob, keep = _gpu(val, count, temperature, top_p, dtype)
+    _compare(prob, keep, val, count, temperature, top_p, what, dtype)
 
 
-def _compare(prob, keep, val, count, temperature: float, top_p: float, what: str):
+def _compare(prob, keep, val, count, temperature: float, top_p: float, what: str, dtype: str = "bf16"):
     # the kernel sees the float32 values of T and top_p
     t32, p32 = float(np.float32(temperature)), float(np.float32(top_p))
-    ref_prob, ref_keep, soft = nucleus(val, count, t32, p32)
+    ref_prob, ref_keep, soft = nucleus(val, count, t32, p32, dtype=dtype)
     rows, k = val.shape
     assert prob.shape == (rows, k) and keep.shape == (rows,)
     moved = 0
@@ -65,7 +72,7 @@ def _compare(prob, keep, val, count, temperature: float, top_p: float, what: str
             assert cum[m - 1] >= p32 - DELTA and (m == 1 or cum[m - 2] < p32 + DELTA), \
                 f"{what} row {r}: keep {m} is not a valid cut (oracle {m_ref})"
             n = max(0, min(k, int(count[r])))
-            vals = [bf16_value(b) for b in val[r, :n]]
+            vals = [float(x) for x in values_of(val[r, :n], dtype)]
             exp = np.zeros(k)
             exp[:n] = nucleus_row(vals, t32, p32, keep=m)[2]
             moved += 1
@@ -127,3 +134,16 @@ def test_rows_beyond_one_block_and_counts_out_of_range():
     count[(count == 20) & (rows % 3 == 0)] = 25     # full lists: entries past k do not exist
     count[3::11] = -4
     _check(val, count, 0.7, 0.95, "clamped counts")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+@pytest.mark.parametrize("temperature,top_p", [(0.7, 0.95), (0.0, 0.95), (1.0, 0.9), (5.0, 1.0)])
+def test_other_formats(dtype, temperature, top_p):
+    """The same ranked lists as fp16 (rounded) and fp32 (widened) values: the
+    order survives (rounding is monotone), NaN and infinities map to the
+    format's own."""
+    val, count = synth.ranked_lists(600, 20, seed=321)
+    vals = synth.bf16_to_float(val)
+    with np.errstate(over="ignore", invalid="ignore"):
+        bits = vals.astype(np.float16).view(np.uint16) if dtype == "f16" else np.ascontiguousarray(vals).view(np.uint32)
+    _check(bits, count, temperature, top_p, f"{dtype} T{temperature} p{top_p}", dtype)

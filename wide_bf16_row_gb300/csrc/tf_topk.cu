@@ -58,6 +58,7 @@
 // cluster barrier or the last-arriver ticket.
 
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -1583,8 +1584,19 @@ __device__ __forceinline__ float warp_inclusive_scan(float x, int lane)
     return x;
 }
 
+// A list value as float (exact for every format): bf16 is the top half of a
+// binary32, fp16 widens exactly, fp32 is itself.
+template <int kFmt>
+__device__ __forceinline__ float list_value(uint32_t bits)
+{
+    if constexpr (kFmt == TF_TOPK_DTYPE_F16) return __half2float(__ushort_as_half((unsigned short)bits));
+    else if constexpr (kFmt == TF_TOPK_DTYPE_F32) return __uint_as_float(bits);
+    else return __uint_as_float(bits << 16);
+}
+
+template <typename T, int kFmt>
 __global__ void __launch_bounds__(kNucleusWarps * 32)
-topk_nucleus_kernel(const uint16_t *__restrict__ val, const int32_t *__restrict__ count, int64_t rows, int32_t k,
+topk_nucleus_kernel(const T *__restrict__ val, const int32_t *__restrict__ count, int64_t rows, int32_t k,
                     float temperature, float top_p, float *__restrict__ out_prob, int32_t *__restrict__ out_keep)
 {
     grid_dependency_wait();
@@ -1597,7 +1609,7 @@ topk_nucleus_kernel(const uint16_t *__restrict__ val, const int32_t *__restrict_
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         const int i = lane + 32 * j;
-        v[j] = i < n_in ? __uint_as_float((uint32_t)val[r * k + i] << 16) : 0.f;
+        v[j] = i < n_in ? list_value<kFmt>((uint32_t)val[r * k + i]) : 0.f;
         nan[j] = i < n_in && isnan(v[j]);
     }
     // the top-k ranks NaN below every number: the numbers are the prefix before the first NaN
@@ -2485,16 +2497,36 @@ int run_merge(const int32_t *in_idx, const uint16_t *in_val, const int32_t *in_c
     return TF_TOPK_OK;
 }
 
-// tf_topk_nucleus_bf16: argument checks, then one warp per row.
-int run_nucleus(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature, float top_p,
-                float *out_prob, int32_t *out_keep, void *stream)
+// tf_topk_nucleus / tf_topk_nucleus_bf16: argument checks, then one warp per row.
+template <typename T, int kFmt>
+cudaError_t launch_nucleus(const T *val, const int32_t *count, int64_t r0, int64_t nr, int32_t k, float temperature,
+                           float top_p, float *out_prob, int32_t *out_keep, cudaStream_t strm)
 {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((nr + kNucleusWarps - 1) / kNucleusWarps), 1, 1);
+    cfg.blockDim = dim3(kNucleusWarps * 32, 1, 1);
+    cfg.stream = strm;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_nucleus_kernel<T, kFmt>, val + r0 * k, count + r0, nr, k, temperature,
+                              top_p, out_prob + r0 * k, out_keep + r0);
+}
+
+int run_nucleus(const void *val, int32_t dtype, const int32_t *count, int64_t rows, int32_t k, float temperature,
+                float top_p, float *out_prob, int32_t *out_keep, void *stream)
+{
+    if (dtype != TF_TOPK_DTYPE_BF16 && dtype != TF_TOPK_DTYPE_F16 && dtype != TF_TOPK_DTYPE_F32)
+        return TF_TOPK_ERR_DTYPE;
     if (k < 1 || k > kMaxK) return TF_TOPK_ERR_K;
     if (rows < 0) return TF_TOPK_ERR_SHAPE;
     if (!(temperature >= 0.f) || std::isinf(temperature) || !(top_p > 0.f && top_p <= 1.f)) return TF_TOPK_ERR_ARG;
     if (rows == 0) return TF_TOPK_OK;
     if (!val || !count || !out_prob || !out_keep) return TF_TOPK_ERR_NULL;
-    if ((reinterpret_cast<uintptr_t>(val) & 1) || (reinterpret_cast<uintptr_t>(count) & 3) ||
+    const uintptr_t esz = dtype == TF_TOPK_DTYPE_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(val) & (esz - 1)) || (reinterpret_cast<uintptr_t>(count) & 3) ||
         (reinterpret_cast<uintptr_t>(out_prob) & 3) || (reinterpret_cast<uintptr_t>(out_keep) & 3))
         return TF_TOPK_ERR_ALIGN;
     int dev = 0, sm_count = 0;
@@ -2504,17 +2536,16 @@ int run_nucleus(const uint16_t *val, const int32_t *count, int64_t rows, int32_t
     const int64_t max_rows = (int64_t)INT32_MAX * kNucleusWarps;
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
         const int64_t nr = rows - r0 < max_rows ? rows - r0 : max_rows;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((nr + kNucleusWarps - 1) / kNucleusWarps), 1, 1);
-        cfg.blockDim = dim3(kNucleusWarps * 32, 1, 1);
-        cfg.stream = strm;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_nucleus_kernel, val + r0 * k, count + r0, nr, k, temperature,
-                                           top_p, out_prob + r0 * k, out_keep + r0);
+        cudaError_t e;
+        if (dtype == TF_TOPK_DTYPE_F32)
+            e = launch_nucleus<uint32_t, TF_TOPK_DTYPE_F32>(static_cast<const uint32_t *>(val), count, r0, nr, k,
+                                                            temperature, top_p, out_prob, out_keep, strm);
+        else if (dtype == TF_TOPK_DTYPE_F16)
+            e = launch_nucleus<uint16_t, TF_TOPK_DTYPE_F16>(static_cast<const uint16_t *>(val), count, r0, nr, k,
+                                                            temperature, top_p, out_prob, out_keep, strm);
+        else
+            e = launch_nucleus<uint16_t, TF_TOPK_DTYPE_BF16>(static_cast<const uint16_t *>(val), count, r0, nr, k,
+                                                             temperature, top_p, out_prob, out_keep, strm);
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return fail_cuda(e);
     }
@@ -2681,7 +2712,13 @@ int tf_topk_merge_bf16(const int32_t *in_idx, const uint16_t *in_val, const int3
 int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows, int32_t k, float temperature,
                          float top_p, float *out_prob, int32_t *out_keep, void *stream)
 {
-    return run_nucleus(val, count, rows, k, temperature, top_p, out_prob, out_keep, stream);
+    return run_nucleus(val, TF_TOPK_DTYPE_BF16, count, rows, k, temperature, top_p, out_prob, out_keep, stream);
+}
+
+int tf_topk_nucleus(const void *val, int32_t dtype, const int32_t *count, int64_t rows, int32_t k, float temperature,
+                    float top_p, float *out_prob, int32_t *out_keep, void *stream)
+{
+    return run_nucleus(val, dtype, count, rows, k, temperature, top_p, out_prob, out_keep, stream);
 }
 
 int tf_topk_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,

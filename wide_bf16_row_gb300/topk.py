@@ -61,6 +61,8 @@ def library() -> ctypes.CDLL:
         lib.tf_topk_bf16_noalloc.argtypes = [c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
         lib.tf_topk_nucleus_bf16.restype = ctypes.c_int
         lib.tf_topk_nucleus_bf16.argtypes = [c_p, c_p, c_i64, c_i32, ctypes.c_float, ctypes.c_float, c_p, c_p, c_p]
+        lib.tf_topk_nucleus.restype = ctypes.c_int
+        lib.tf_topk_nucleus.argtypes = [c_p, c_i32, c_p, c_i64, c_i32, ctypes.c_float, ctypes.c_float, c_p, c_p, c_p]
         lib.tf_topk_select.restype = ctypes.c_int
         lib.tf_topk_select.argtypes = [c_p, c_i32, c_i64, c_i64, c_i64, c_i32, c_p, c_p, c_p, c_p, c_p]
         lib.tf_topk_select_with_plan.restype = ctypes.c_int
@@ -179,6 +181,12 @@ def tf_topk_nucleus_bf16(val: int, count: int, rows: int, k: int, temperature: f
     return library().tf_topk_nucleus_bf16(val, count, rows, k, temperature, top_p, out_prob, out_keep, stream)
 
 
+def tf_topk_nucleus(val: int, dtype: int, count: int, rows: int, k: int, temperature: float, top_p: float,
+                    out_prob: int, out_keep: int, stream: int | None) -> int:
+    """The C nucleus (top-p) entry point for lists of any format; returns the status code."""
+    return library().tf_topk_nucleus(val, dtype, count, rows, k, temperature, top_p, out_prob, out_keep, stream)
+
+
 def nucleus_bf16(val, count, temperature: float, top_p: float, *, out=None, stream=None):
     """Sampling probabilities over top-k lists (softmax of value / T, then the
     shortest best-first prefix with mass >= top_p, renormalised).
@@ -187,8 +195,23 @@ def nucleus_bf16(val, count, temperature: float, top_p: float, *, out=None, stre
     returns them (contiguous CUDA tensors).  Returns (prob float32 [rows, k],
     keep int32 [rows]).
     """
+    return nucleus(val, count, temperature, top_p, dtype=DTYPE_BF16, out=out, stream=stream)
+
+
+def nucleus(val, count, temperature: float, top_p: float, *, dtype: int | None = None, out=None, stream=None):
+    """``nucleus_bf16`` for lists of any format ``select_topk`` returns:
+    val bfloat16 / float16 / float32 [rows, k] (or int16 / int32 bits with
+    ``dtype``), count int32 [rows]."""
     import torch
 
+    codes = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32,
+             torch.int16: DTYPE_BF16, torch.uint16: DTYPE_BF16, torch.int32: DTYPE_F32}
+    if dtype is None:
+        if val.dtype not in codes:
+            raise TypeError(f"unsupported list dtype {val.dtype}")
+        dtype = codes[val.dtype]
+    if val.element_size() != (4 if dtype == DTYPE_F32 else 2):
+        raise TypeError("element size does not match dtype")
     if val.dim() != 2 or count.dim() != 1 or count.shape[0] != val.shape[0]:
         raise ValueError("val must be [rows, k] and count [rows]")
     for t in (val, count):
@@ -200,8 +223,8 @@ def nucleus_bf16(val, count, temperature: float, top_p: float, *, out=None, stre
                torch.empty((rows,), dtype=torch.int32, device=val.device))
     if stream is None:
         stream = torch.cuda.current_stream(val.device)
-    _check(tf_topk_nucleus_bf16(val.data_ptr(), count.data_ptr(), rows, k, float(temperature), float(top_p),
-                                out[0].data_ptr(), out[1].data_ptr(), stream.cuda_stream))
+    _check(tf_topk_nucleus(val.data_ptr(), dtype, count.data_ptr(), rows, k, float(temperature), float(top_p),
+                           out[0].data_ptr(), out[1].data_ptr(), stream.cuda_stream))
     return out
 
 
