@@ -62,6 +62,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 
 #include <map>
@@ -2558,15 +2559,17 @@ template <typename T, int kFmt, int Q>
 int launch_wide(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k, int32_t *out_idx,
                 void *out_val, int32_t *out_count, uint32_t *out_mask, cudaStream_t strm)
 {
-    static bool attr_done[kMaxDevices];
+    // per device, once (setting the attribute twice from racing threads is harmless)
+    static std::atomic<bool> attr_done[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e);
-    if (!attr_done[dev]) {
+    if (dev < 0 || dev >= kMaxDevices) return TF_TOPK_ERR_DEVICE;
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(topk_wide_kernel<T, kFmt, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)sizeof(WideSmem));
         if (e != cudaSuccess) return fail_cuda(e);
-        attr_done[dev] = true;
+        attr_done[dev].store(true, std::memory_order_release);
     }
     const T *x = static_cast<const T *>(logits);
     T *ov = static_cast<T *>(out_val);
