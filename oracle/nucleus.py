@@ -31,11 +31,6 @@ import math
 import numpy as np
 
 
-def bf16_value(bits: int) -> float:
-    """The real value of bf16 bits (exact)."""
-    return float(np.array([int(bits) << 16], dtype=np.uint32).view(np.float32)[0])
-
-
 def nucleus_row(vals: list[float], temperature: float, top_p: float,
                 keep: int | None = None) -> tuple[list[float], int, list[float]]:
     """One row: (probabilities of every entry, kept count, renormalised kept

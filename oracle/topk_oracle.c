@@ -314,12 +314,3 @@ int oracle_topk(const void *logits, int32_t dtype, int64_t rows, int64_t cols, i
     free(tids);
     return status;
 }
-
-/* The bf16 entry: oracle_topk with dtype 0. */
-int oracle_topk_bf16(const uint16_t *logits, int64_t rows, int64_t cols, int64_t row_stride,
-                     int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
-                     uint32_t *out_mask, int32_t nthreads)
-{
-    return oracle_topk(logits, ORACLE_BF16, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
-                       nthreads);
-}

@@ -9,7 +9,7 @@ import math
 import numpy as np
 import pytest
 
-from oracle.nucleus import nucleus, nucleus_row
+from oracle.nucleus import nucleus, nucleus_row, values_of
 
 
 def test_two_values_follow_the_logistic_closed_form():
@@ -104,7 +104,6 @@ def test_a_fixed_keep_replaces_the_cut():
 
 def test_other_formats_decode_exactly():
     """fp16 and fp32 lists: the same steps on exactly decoded values."""
-    from oracle.nucleus import values_of
     assert values_of(np.array([0x3C00, 0x0001, 0xFC00], np.uint16), "f16").tolist() == [1.0, 2.0 ** -24, -math.inf]
     assert values_of(np.array([0x3F800001], np.uint32), "f32")[0] == 1.0 + 2.0 ** -23
     assert values_of(np.array([0x4040], np.uint16))[0] == 3.0
@@ -114,3 +113,14 @@ def test_other_formats_decode_exactly():
     f16 = np.array([[0x3C00, 0x3C00, 0x3C00, 0x7E00]], np.uint16)    # 1, 1, 1, NaN
     prob, keep, soft = nucleus(f16, np.array([4]), 0.7, 0.5, dtype="f16")
     assert keep.tolist() == [2] and soft[0].tolist() == pytest.approx([1 / 3, 1 / 3, 1 / 3, 0.0])
+
+
+def test_counts_outside_the_list_are_clamped():
+    """A list holds k entries: a count above k reads k of them, a negative one none."""
+    bits = np.array([[0x4040, 0x3F80, 0x3F80]], dtype=np.uint16)           # 3, 1, 1
+    ref = nucleus(bits, np.array([3]), 0.7, 0.9)
+    over = nucleus(bits, np.array([7]), 0.7, 0.9)
+    for a, b in zip(ref, over):
+        np.testing.assert_array_equal(a, b)
+    prob, keep, soft = nucleus(bits, np.array([-2]), 0.7, 0.9)
+    assert keep.tolist() == [0] and not prob.any() and not soft.any()

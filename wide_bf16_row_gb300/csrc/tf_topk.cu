@@ -376,7 +376,6 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
 struct ChunkGeom {
     const uint16_t *rowp;
     int32_t cols, m, vfull0, vfull1;
-    int32_t cbeg, cend; // chunk vectors
 };
 
 __device__ __forceinline__ ChunkGeom row_geometry(const uint16_t *rowp, int32_t cols)
@@ -387,7 +386,6 @@ __device__ __forceinline__ ChunkGeom row_geometry(const uint16_t *rowp, int32_t 
     g.m = (int32_t)((reinterpret_cast<uintptr_t>(rowp) >> 1) & 7);
     g.vfull0 = g.m ? 1 : 0;
     g.vfull1 = (cols + g.m) >> 3;
-    g.cbeg = g.cend = 0;
     return g;
 }
 
@@ -1428,11 +1426,7 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         // a full chunk inside the row: the max from the raw bits where it can be
         uint32_t tmax = 0;
         const bool raw = full && raw_tmax<kFmt>(kv, tmax);
-        if (!raw) {
-            geo.cbeg = cbeg;
-            geo.cend = cend;
-            tmax = chunk_keys<false, kFmt>(kv, nvalid, col_base, cols, keys, sm);
-        }
+        if (!raw) tmax = chunk_keys<false, kFmt>(kv, nvalid, col_base, cols, keys, sm);
         const uint32_t t_floor = chunk_floor(tmax, nvalid, k, sm, run_i, run_len);
         const bool hit = spill_hits(kv, tmax, raw, t_floor, keys);
         // the chunk's registers are free: the next chunk's loads fly during
