@@ -227,6 +227,142 @@ def workload_config(w, extra: dict | None = None) -> dict:
     return cfg
 
 
+def isolated_launches(step, stream, dev, n: int) -> list[float]:
+    """n launches, each alone between its own pair of events (synchronised
+    before and after, so none overlaps a neighbour); ms per launch."""
+    import torch
+
+    out = []
+    for i in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        step(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append(a.elapsed_time(b))
+    return out
+
+
+# The workloads the per-config table covers: the four named ones and sweep points.
+PER_CONFIG = (
+    ("1x4096_k8", None),
+    ("15x98592_k16", None),
+    ("16x248320_k64_specials", None),
+    ("256x248320_k20", None),
+    ("sweep_1024x248320_k20", (248320, 1024, 20)),
+    ("sweep_64x151936_k64", (151936, 64, 64)),
+    ("sweep_4x98592_k8", (98592, 4, 8)),
+    ("sweep_1024x4096_k20", (4096, 1024, 20)),
+)
+
+
+def per_config_workload(name: str, sweep):
+    from wide_bf16_row_gb300 import synth
+
+    return synth.config_sweep(*sweep) if sweep else synth.NAMED[name]()
+
+
+def measure_config(w, dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:
+    """One workload through tf_topk_bf16 (the library's own plan): kernel time
+    per call from a CUDA graph of back-to-back calls (no host issue cost),
+    inputs rotating over copies that together exceed L2 four times where that
+    fits (small inputs stay L2-resident, said in `l2`); the same calls issued
+    from Python; single isolated calls; the host cost of one call; and the
+    oracle on the host cores."""
+    import torch
+
+    from wide_bf16_row_gb300 import topk
+
+    rows, cols, stride, k = w.rows, w.cols, w.row_stride, w.k
+    in_bytes = rows * stride * 2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    want = max(2, math.ceil(4 * l2 / in_bytes))
+    nbuf = min(want, 64)
+    host = torch.from_numpy(w.logits.view(np.int16))
+    bufs = [host.to(dev) for _ in range(nbuf)]
+    views = [b.as_strided((rows, cols), (stride, 1)) for b in bufs]
+    out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
+           torch.empty((rows, k), dtype=torch.int16, device=dev),
+           torch.empty((rows,), dtype=torch.int32, device=dev),
+           torch.empty((rows,), dtype=torch.int32, device=dev))
+    plan = topk.plan(rows, cols, k)
+    side = torch.cuda.Stream(dev)
+
+    def call(i, s):
+        topk.topk_bf16(views[i % nbuf], k, out=out, stream=s)
+
+    with torch.cuda.stream(side):
+        for i in range(5):
+            call(i, side)
+    torch.cuda.synchronize(dev)
+    # kernel time: a graph of G back-to-back calls, replayed R times
+    n_calls = max(2 * nbuf, 40)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for i in range(n_calls):
+            call(i, side)
+    reps = max(3, min(200, int(2e5 / max(1.0, n_calls))))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):  # a graph replays on the current stream
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        a.record(side)
+        for _ in range(reps):
+            graph.replay()
+        b.record(side)
+    torch.cuda.synchronize(dev)
+    us_graph = a.elapsed_time(b) * 1e3 / (reps * n_calls)
+    # the same calls issued from Python, back to back
+    n_py = 200
+    a.record(side)
+    for i in range(n_py):
+        call(i, side)
+    b.record(side)
+    torch.cuda.synchronize(dev)
+    us_python = a.elapsed_time(b) * 1e3 / n_py
+    # host cost of one call (argument checks, plan, launch): no synchronisation
+    t0 = time.perf_counter()
+    for i in range(n_py):
+        call(i, side)
+    host_us = (time.perf_counter() - t0) * 1e6 / n_py
+    torch.cuda.synchronize(dev)
+    iso = [x * 1e3 for x in isolated_launches(lambda i: call(i, side), side, dev, 30)]
+    alg = rows * cols * 2 + rows * k * 6 + rows * 8
+    gbs = alg / (us_graph * 1e-6) / 1e9
+    res = {
+        "rows": rows, "cols": cols, "k": k, "row_stride": stride,
+        "plan": PLAN_NAME.get(plan, str(plan)),
+        "us_per_call": us_graph,
+        "rows_per_s": rows / (us_graph * 1e-6),
+        "gbs": gbs, "frac_of_peak": gbs / peak,
+        "algorithmic_bytes": alg,
+        "us_per_call_python_issued": us_python,
+        "us_isolated_p10_p50_p90": [round(float(np.percentile(iso, q)), 2) for q in (10, 50, 90)],
+        "host_us_per_call": host_us,
+        "timing": f"CUDA graph of {n_calls} back-to-back calls, {reps} replays, CUDA events",
+        "l2": (f"inputs rotate over {nbuf} device copies ({nbuf * in_bytes / 1e6:.0f} MB)"
+               + ("" if nbuf >= want else "; fits L2 (L2-resident)")),
+    }
+    if cpu:
+        all_cores = time_oracle(w, budget_s=cpu_seconds)
+        one = time_oracle(w, budget_s=cpu_seconds / 2, rows_per_call=1)
+        res["oracle_rows_per_s"] = all_cores["value"]
+        res["oracle_cores"] = all_cores["cores"]
+        res["oracle_rows_per_s_1core"] = one["value"]
+    del bufs, views
+    torch.cuda.empty_cache()
+    return res
+
+
+def per_config_table(dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:
+    table = {}
+    for name, sweep in PER_CONFIG:
+        w = per_config_workload(name, sweep)
+        table[name] = measure_config(w, dev, peak, cpu, cpu_seconds)
+    return table
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 def time_oracle(w, budget_s: float, rows_per_call: int | None = None, bits: np.ndarray | None = None,
@@ -354,12 +490,8 @@ def run_ours(args) -> None:
         step(i)
     torch.cuda.synchronize(dev)
 
-    # the launches run back to back (each may be scheduled while the previous one
-    # finishes); a sparse subset is also timed alone between its own events
-    every = max(64, args.steps // 64)
-    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for i in range(0, args.steps, every)}
-
+    # the timed launches run back to back (each may be scheduled while the
+    # previous one finishes); isolated launches are timed afterwards, apart
     sampler = ClockSampler(nvsmi_id(dev)) if not args.no_clocks else None
     if sampler:
         sampler.wait_first()
@@ -370,12 +502,7 @@ def run_ours(args) -> None:
     t0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        e = ev.get(i)
-        if e:
-            e[0].record(stream)
         step(i)
-        if e:
-            e[1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
@@ -385,7 +512,7 @@ def run_ours(args) -> None:
     if sampler:
         sampler.stop()
     elapsed_ms = start.elapsed_time(end)
-    launch_ms = [a.elapsed_time(b) for a, b in ev.values()]
+    launch_ms = isolated_launches(step, stream, dev, n=min(50, max(3, args.steps)))
 
     # L2-warm: the same input every call (draft logits often sit in L2 right
     # after the head that wrote them); reported beside the L2-cold value
@@ -441,6 +568,10 @@ def run_ours(args) -> None:
     h2d = rows * stride * esize
     d2h = rows * k * 4 + rows * k * esize + rows * 4 + rows * 4
 
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per_config = per_config_table(dev, peak, not args.no_cpu_baseline, min(0.6, args.cpu_seconds))
+
     cpu = None
     cpu_1core = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -485,6 +616,7 @@ def run_ours(args) -> None:
             "clocks": clocks,
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu_1core,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -507,6 +639,8 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload table (every named workload and sweep points)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

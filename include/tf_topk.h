@@ -29,10 +29,12 @@
  *
  * Every call is asynchronous on the given stream and returns after the launch;
  * device faults, if any, surface at the caller's next synchronisation.  The
- * library allocates no output and keeps no per-call state beyond its
- * per-stream scratch, so calls on different streams and host threads may
- * overlap.  On an error return nothing has been
- * launched and no output has been written.
+ * library allocates no output.  The allocating entry points keep no per-call
+ * state beyond their per-stream scratch, so their calls on different streams
+ * and host threads may overlap.  The exception is tf_topk_bf16_noalloc, whose
+ * calls all share one static scratch array and must not overlap on the GPU
+ * (see its section).  On an error return nothing has been launched and no
+ * output has been written.
  */
 #ifndef TF_TOPK_H
 #define TF_TOPK_H
@@ -88,7 +90,9 @@ extern "C" {
  * per-(device, stream) area (two k-entry lists and a ticket per CTA, under
  * 1 MB) that the library allocates on its first call on that stream and keeps
  * until exit; that first call therefore allocates (cudaMalloc) and should not
- * be made during stream capture.  Outputs are never allocated by the library.
+ * be made during stream capture.  Each stream-plan launch first clears the
+ * tickets it uses with an asynchronous memset on `stream`.  Outputs are never
+ * allocated by the library.
  */
 int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
                  int32_t *out_idx, uint16_t *out_val, int32_t *out_count,

@@ -1,4 +1,4 @@
-"""The allocation-free entry point, tf_topk_bf16_noalloc, against tf_topk_bf16.
+"""The allocation-free entry point, tf_topk_bf16_noalloc, against the CPU oracle.
 
 Some callers cannot allocate device memory once they run: a serving engine
 that has reserved nearly all of HBM for its caches, or a host of custom
@@ -6,8 +6,9 @@ operators that only passes in the buffers it owns.  For them the library keeps
 its scratch in one static device array instead of allocating it per stream.
 These checks call that entry point through the C ABI, two calls in a row on
 one stream (the second reuses the array the first left behind), and require
-byte-equal results with the ordinary entry point -- the same bar as every
-other parity test here.
+byte-equal results with the CPU oracle -- the same bar as every other parity
+test here.  One more check shows that the calls allocate nothing: the
+device's free memory is the same before and after two calls on a new stream.
 
 The file name sorts last, so a run that stops at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -16,6 +17,7 @@ from __future__ import annotations
 
 import pytest
 
+import oracle
 from tests.gpu_util import assert_same, device_matrix, to_numpy
 from wide_bf16_row_gb300 import synth
 
@@ -53,22 +55,43 @@ def _inputs():
 
 
 @pytest.mark.parametrize("w", list(_inputs()), ids=lambda w: w.name)
-def test_two_calls_in_a_row_match_the_allocating_entry(w):
+def test_two_calls_in_a_row_match_the_oracle(w):
     import torch
 
     from wide_bf16_row_gb300 import topk
 
     view, keep = device_matrix(w.logits, w.cols)
     s = torch.cuda.current_stream()
-    ref = _outputs(w.rows, w.k)
-    assert _call(topk.tf_topk_bf16, view, w.k, ref, s) == topk.OK
+    exp = oracle.topk(w.logits, w.cols, w.k)
     first, second = _outputs(w.rows, w.k, fill=7), _outputs(w.rows, w.k, fill=9)
     assert _call(topk.tf_topk_bf16_noalloc, view, w.k, first, s) == topk.OK
     assert _call(topk.tf_topk_bf16_noalloc, view, w.k, second, s) == topk.OK
-    exp = to_numpy(ref)
     assert_same(to_numpy(first), exp, f"{w.name} first no-alloc call")
     assert_same(to_numpy(second), exp, f"{w.name} second no-alloc call")
     assert topk.device_fault() == 0
+    del keep
+
+
+def test_calls_allocate_no_device_memory():
+    """After one warm call (it loads the kernel and looks up the array's
+    address), two more calls on a stream created for them leave the device's
+    free memory unchanged."""
+    import torch
+
+    from wide_bf16_row_gb300 import topk
+
+    w = synth.config_draft_window()
+    view, keep = device_matrix(w.logits, w.cols)
+    out = _outputs(w.rows, w.k)
+    assert _call(topk.tf_topk_bf16_noalloc, view, w.k, out, torch.cuda.current_stream()) == topk.OK
+    fresh = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(2):
+        assert _call(topk.tf_topk_bf16_noalloc, view, w.k, out, fresh) == topk.OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert_same(to_numpy(out), oracle.topk(w.logits, w.cols, w.k), "no-alloc call on a new stream")
     del keep
 
 
@@ -82,14 +105,11 @@ def test_back_to_back_calls_on_different_shapes():
     va, ka = device_matrix(a.logits, a.cols)
     vb, kb = device_matrix(b.logits, b.cols)
     s = torch.cuda.current_stream()
-    ra, rb = _outputs(a.rows, a.k), _outputs(b.rows, b.k)
-    assert _call(topk.tf_topk_bf16, va, a.k, ra, s) == topk.OK
-    assert _call(topk.tf_topk_bf16, vb, b.k, rb, s) == topk.OK
     na, nb = _outputs(a.rows, a.k, fill=3), _outputs(b.rows, b.k, fill=3)
     assert _call(topk.tf_topk_bf16_noalloc, va, a.k, na, s) == topk.OK
     assert _call(topk.tf_topk_bf16_noalloc, vb, b.k, nb, s) == topk.OK
-    assert_same(to_numpy(na), to_numpy(ra), "256x248320 then ...")
-    assert_same(to_numpy(nb), to_numpy(rb), "... 15x98592")
+    assert_same(to_numpy(na), oracle.topk(a.logits, a.cols, a.k), "256x248320 then ...")
+    assert_same(to_numpy(nb), oracle.topk(b.logits, b.cols, b.k), "... 15x98592")
     del ka, kb
 
 

@@ -272,15 +272,23 @@ __device__ __forceinline__ uint32_t block_sum(uint32_t v, SmemCore &sm, int pari
     return s;
 }
 
-// The candidate counter only grows within a chunk loop: a chunk's slots count
-// from `base`, the counter's value when the chunk began.
-__device__ __forceinline__ void push_candidate(SmemCore &sm, uint32_t key, int local, uint32_t base)
+// A candidate at a given slot (chunk-relative); slots past the buffer are
+// not written.
+__device__ __forceinline__ void put_candidate(SmemCore &sm, uint32_t key, int local, uint32_t slot)
 {
-    const uint32_t slot = atomicAdd(&sm.n_cand, 1u) - base;
     if (slot < (uint32_t)kCandCap) {
         sm.cand[slot] = (canon(key) << 16) | (0xFFFFu - (uint32_t)local);
         sm.cand_raw[slot] = (uint16_t)raw_from_key(key);
     }
+}
+
+// The candidate counter only grows within a chunk loop: a chunk's slots count
+// from `base`, the counter's value when the chunk began.  Returns the slot.
+__device__ __forceinline__ uint32_t push_candidate(SmemCore &sm, uint32_t key, int local, uint32_t base)
+{
+    const uint32_t slot = atomicAdd(&sm.n_cand, 1u) - base;
+    put_candidate(sm, key, local, slot);
+    return slot;
 }
 
 // Keys of the staged chunk whose score is >= the score of key t (t >= 1), this
@@ -300,8 +308,9 @@ __device__ __forceinline__ uint32_t count_at_least(const uint32_t *keys, uint32_
 // Exact selection for a chunk whose candidate set {key >= t_floor} is larger
 // than the candidate buffer (heavy ties, e.g. an all-zero row).  The chunk's
 // keys have been staged in `keys` in column order (0 = not a candidate).
-// Writes exactly k candidates -- the chunk's top-k within that set -- into
-// sm.cand.  Block-uniform; every thread calls it.
+// Writes the chunk's top-k within that set -- k candidates, or all of them
+// when fewer reach t_floor -- into sm.cand, and their number into sm.n_cand.
+// Block-uniform; every thread calls it.
 template <int kFmt = kBf16>
 __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor, int k, SmemCore &sm)
 {
@@ -309,10 +318,11 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
     // 1. K* = the largest canonical key that at least k elements reach.
     uint32_t my_max = 0;
     for (int w = tid; w < kChunkCols / 2; w += kThreads)
-        my_max = max(my_max, max(keys[w] & 0xFFFFu, keys[w] >> 16));
+        my_max = max(my_max, max(canon(keys[w] & 0xFFFFu), canon(keys[w] >> 16)));
+    my_max = __reduce_max_sync(0xFFFFFFFFu, my_max);
     if (tid == 0) sm.kmax = 0;
     __syncthreads();
-    atomicMax(&sm.kmax, canon(my_max));
+    if ((tid & 31) == 0) atomicMax(&sm.kmax, my_max);
     __syncthreads();
     uint32_t lo = canon(t_floor); // count(lo) > kCandCap >= k
     uint32_t hi = sm.kmax + 1;    // count(hi) == 0
@@ -327,44 +337,55 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
             hi = mid;
     }
     const uint32_t kstar = lo;
-    const uint32_t above =
-        (kstar >= Fmt16<kFmt>::kKeyPosInf) ? 0u : block_sum(count_at_least(keys, kstar + 1), sm, parity);
-    const uint32_t need = (uint32_t)k - above; // ties at K* to take, lowest columns first
 
-    // 2. Each thread owns a contiguous run of columns; an exclusive scan of the
-    //    per-thread tie counts gives every tie its rank in column order.
+    // 2. Each thread owns a contiguous run of columns.  One exclusive scan of
+    //    the per-thread counts -- keys above K* in the high half, ties at K* in
+    //    the low half (at most a chunk of them: no carry into the high half) --
+    //    gives every entry its slot: the entries above K* first, then the
+    //    lowest columns among the ties, as many as the k places left.
     constexpr int kWordsPerThread = kChunkCols / 2 / kThreads;
     const int w0 = tid * kWordsPerThread;
-    uint32_t ties = 0;
+    uint32_t mine = 0;
     for (int w = w0; w < w0 + kWordsPerThread; ++w) {
-        ties += canon(keys[w] & 0xFFFFu) == kstar;
-        ties += canon(keys[w] >> 16) == kstar;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t c = canon(h ? (keys[w] >> 16) : (keys[w] & 0xFFFFu)); // key 0 is never >= K* >= 1
+            mine += c > kstar ? 0x10000u : (c == kstar ? 1u : 0u);
+        }
     }
     const int lane = tid & 31, warp = tid >> 5;
-    uint32_t incl = ties;
+    uint32_t incl = mine;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
         if (lane >= d) incl += u;
     }
     if (lane == 31) sm.scan[warp][0] = incl;
-    if (tid == 0) sm.n_cand = 0;
     __syncthreads();
-    uint32_t ord = incl - ties;
-    for (int w = 0; w < warp; ++w) ord += sm.scan[w][0];
+    uint32_t excl = incl - mine, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t t = sm.scan[w][0];
+        excl += w < warp ? t : 0u;
+        total += t;
+    }
+    const uint32_t above = total >> 16;                     // < k: K* is the k-th largest key
+    const uint32_t need = (uint32_t)k - above;              // ties to take, lowest columns first
+    const uint32_t taken = min(need, total & 0xFFFFu);      // fewer when fewer than k keys reach t_floor
+    if (tid == 0) sm.n_cand = above + taken;
 
-    // 3. Collect everything above K* and the first `need` ties.
+    // 3. Place them.
+    uint32_t a_ord = excl >> 16, t_ord = excl & 0xFFFFu;
     for (int w = w0; w < w0 + kWordsPerThread; ++w) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const uint32_t key = h ? (keys[w] >> 16) : (keys[w] & 0xFFFFu);
-            if (key == 0) continue;
             const uint32_t c = canon(key);
             if (c > kstar) {
-                push_candidate(sm, key, 2 * w + h, 0u);
+                put_candidate(sm, key, 2 * w + h, a_ord++);
             } else if (c == kstar) {
-                if (ord < need) push_candidate(sm, key, 2 * w + h, 0u);
-                ++ord;
+                if (t_ord < need) put_candidate(sm, key, 2 * w + h, above + t_ord);
+                ++t_ord;
             }
         }
     }
@@ -406,7 +427,7 @@ __device__ __noinline__ uint4 load_edge_vector(const uint16_t *rowp, int32_t col
 }
 
 // The exact key pass for one thread whose chunk slice holds a column outside
-// the row or a non-finite value.  Its keys sit in its own stage slots
+// the row (its keys may also hold non-finite values).  Its keys sit in its own stage slots
 // (vector i at stage[i * kThreads + tid]); columns outside the row and NaNs
 // become key 0 and the row's non-finite flags are recorded.  Returns the
 // thread's max key over what remains.
@@ -448,15 +469,26 @@ __device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_
 }
 
 // Keys of one chunk.  kv holds the raw words of this thread's vectors (vector
-// i is chunk vector i * kThreads + tid; vectors past the chunk end are 0); on
-// return it holds their keys (0 where no score may be selected), and the
-// thread's max key is returned.  kFull: every vector of the chunk lies wholly
-// inside the row (no predicates).  `stage` is the chunk's 32 KB of shared
-// memory, this thread's slots of which the rare exact pass may use.
+// i is chunk vector cbeg + i * kThreads + tid; vectors past the chunk end are
+// 0); on return it holds their keys (0 where no score may be selected), and
+// the thread's max key is returned.  kFull: every vector of the chunk lies
+// wholly inside the row (no predicates).
+//
+// A thread whose keys reach an infinity's (or below) holds a non-finite value
+// or a column outside the row.  Without the latter, its keys are fixed two at
+// a time in registers: a half is a NaN when its magnitude bits exceed the
+// infinity's (one add into the half's top bit: the sum stays below 2^16, so
+// nothing carries into the other half), and an infinity when its key XOR the
+// infinity's key is zero (the borrow test for a zero half; a borrow into the
+// high half only happens when the low half is itself zero, so "some half is
+// zero" stays exact).  A thread holding an edge vector -- columns outside the
+// row, read as 0xFFFF -- takes the exact per-element pass through its own
+// `stage` slots instead (at most the two vectors at a row's ends).
 template <bool kFull, int kFmt = kBf16>
-__device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4], int nvalid,
-                                               int32_t col_base, int32_t cols, uint4 *stage, SmemCore &sm)
+__device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4], const ChunkGeom &geo, int32_t cbeg,
+                                               int nvalid, uint4 *stage, SmemCore &sm)
 {
+    using F = Fmt16<kFmt>;
     const int tid = threadIdx.x;
     uint32_t mx = 0, mn = 0xFFFFFFFFu;
 #pragma unroll
@@ -473,21 +505,59 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
     }
     uint32_t tmax = max(mx & 0xFFFFu, mx >> 16);
     const uint32_t tmin = min(mn & 0xFFFFu, mn >> 16);
+    if (tmax < F::kKeyPosInf && tmin > F::kKeyNegInf) return tmax;
 
-    // ---- exact key pass (columns outside the row, NaN, +-inf), through shared memory
-    if (tmax >= Fmt16<kFmt>::kKeyPosInf || tmin <= Fmt16<kFmt>::kKeyNegInf) {
-#pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i)
-            stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
-        tmax = fix_keys<kFmt>(stage, col_base, cols, nvalid, sm);
+    bool edge = false;
+    if (!kFull) {
 #pragma unroll
         for (int i = 0; i < kVecPerThread; ++i) {
-            const uint4 q = stage[i * kThreads + tid];
-            kv[i][0] = q.x;
-            kv[i][1] = q.y;
-            kv[i][2] = q.z;
-            kv[i][3] = q.w;
+            const int lv = i * kThreads + tid;
+            const int32_t v = cbeg + lv;
+            edge |= lv < nvalid && (v < geo.vfull0 || v >= geo.vfull1);
         }
+    }
+    if (!edge) {
+        constexpr uint32_t kNanAdd = (0x8000u - (F::kRawPosInf + 1u)) * 0x00010001u;
+        constexpr uint32_t kPosInf2 = F::kKeyPosInf * 0x00010001u, kNegInf2 = F::kKeyNegInf * 0x00010001u;
+        uint32_t nan = 0, pinf = 0, ninf = 0;
+        mx = 0;
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            if (kFull || i * kThreads + tid < nvalid) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t key = kv[i][w];
+                    uint32_t s;
+                    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(s) : "r"(key)); // each half's top bit, spread
+                    const uint32_t mag = (key ^ ~s) & 0x7FFF7FFFu;            // magnitude bits of the value
+                    const uint32_t nb = (mag + kNanAdd) & 0x80008000u;         // a NaN half's top bit
+                    const uint32_t xp = key ^ kPosInf2, xn = key ^ kNegInf2;
+                    nan |= nb;
+                    pinf |= (xp - 0x00010001u) & ~xp;
+                    ninf |= (xn - 0x00010001u) & ~xn;
+                    const uint32_t fixed = key & ~((nb >> 15) * 0xFFFFu);     // NaN -> key 0
+                    kv[i][w] = fixed;
+                    mx = max_u16x2(mx, fixed);
+                }
+            }
+        }
+        const uint32_t flags = (nan ? 1u : 0u) | ((pinf & 0x80008000u) ? 2u : 0u) | ((ninf & 0x80008000u) ? 4u : 0u);
+        if (flags) atomicOr(&sm.flags, flags);
+        return max(mx & 0xFFFFu, mx >> 16);
+    }
+
+    // ---- a row edge in this thread's vectors: the exact pass through shared memory
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i)
+        stage[i * kThreads + tid] = make_uint4(kv[i][0], kv[i][1], kv[i][2], kv[i][3]);
+    tmax = fix_keys<kFmt>(stage, cbeg * 8 - geo.m, geo.cols, nvalid, sm);
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const uint4 q = stage[i * kThreads + tid];
+        kv[i][0] = q.x;
+        kv[i][1] = q.y;
+        kv[i][2] = q.z;
+        kv[i][3] = q.w;
     }
     return tmax;
 }
@@ -638,13 +708,19 @@ __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, 
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncwarp();
-    for (uint32_t hits = __ballot_sync(0xFFFFFFFFu, hit); hits; hits &= hits - 1) {
+    const uint32_t hits0 = __ballot_sync(0xFFFFFFFFu, hit);
+    const bool crowded = __popc(hits0) >= 8; // only then can this warp alone fill the buffer
+    for (uint32_t hits = hits0; hits; hits &= hits - 1) {
         const int src = warp * 32 + __ffs(hits) - 1;
         const int lv = (lane >> 2) * kThreads + src;
         const uint32_t key2 = reinterpret_cast<const uint32_t *>(stage)[lv * 4 + (lane & 3)];
         const int local = lv * 8 + 2 * (lane & 3);
-        if ((key2 & 0xFFFFu) >= t_floor) push_candidate(sm, key2 & 0xFFFFu, local, base);
-        if ((key2 >> 16) >= t_floor) push_candidate(sm, key2 >> 16, local + 1, base);
+        uint32_t top = 0;
+        if ((key2 & 0xFFFFu) >= t_floor) top = push_candidate(sm, key2 & 0xFFFFu, local, base) + 1u;
+        if ((key2 >> 16) >= t_floor) top = push_candidate(sm, key2 >> 16, local + 1, base) + 1u;
+        // past the buffer the chunk is selected exactly from a fresh read:
+        // pushing the rest (up to a whole chunk of ties) would only cost atomics
+        if (crowded && __any_sync(0xFFFFFFFFu, top > (uint32_t)kCandCap)) break;
     }
     __syncthreads();
     const uint32_t total = sm.n_cand;
@@ -846,7 +922,7 @@ __device__ __noinline__ int lazy_overflow(SmemCore &sm, uint64_t *pend, uint4 *s
         kv[i][2] = q.z;
         kv[i][3] = q.w;
     }
-    chunk_keys<false>(kv, nvalid, col_base, geo.cols, stage, sm);
+    chunk_keys<false>(kv, geo, cb, nvalid, stage, sm);
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) {
         uint32_t w[4];
@@ -1218,7 +1294,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                     kv[i][2] = q.z;
                     kv[i][3] = q.w;
                 }
-                tmax = chunk_keys<true>(kv, nvalid, col_base, cols, st, sm);
+                tmax = chunk_keys<true>(kv, geo, cb, nvalid, st, sm);
             } else {
 #pragma unroll
                 for (int i = 0; i < kVecPerThread; ++i) {
@@ -1234,7 +1310,7 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
                     kv[i][2] = q.z;
                     kv[i][3] = q.w;
                 }
-                tmax = chunk_keys<false>(kv, nvalid, col_base, cols, st, sm);
+                tmax = chunk_keys<false>(kv, geo, cb, nvalid, st, sm);
             }
             // A new entry must beat the running k-th strictly once the piece has
             // k entries (every column of this chunk is higher); before that, a
@@ -1426,7 +1502,7 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         // a full chunk inside the row: the max from the raw bits where it can be
         uint32_t tmax = 0;
         const bool raw = full && raw_tmax<kFmt>(kv, tmax);
-        if (!raw) tmax = chunk_keys<false, kFmt>(kv, nvalid, col_base, cols, keys, sm);
+        if (!raw) tmax = chunk_keys<false, kFmt>(kv, geo, cbeg, nvalid, keys, sm);
         const uint32_t t_floor = chunk_floor(tmax, nvalid, k, sm, run_i, run_len);
         const bool hit = spill_hits(kv, tmax, raw, t_floor, keys);
         // the chunk's registers are free: the next chunk's loads fly during
@@ -2170,8 +2246,9 @@ int device_setup(int *dev_out, int *sm_count)
 
 // Scratch of the stream kernel: two partial lists and one ticket per CTA.
 // One area per (device, stream) so that calls on different streams never share
-// it; calls on one stream are ordered by the stream.  Tickets start at zero and
-// every merge puts its ticket back to zero.
+// it; calls on one stream are ordered by the stream.  Every launch clears the
+// tickets it uses first (stream-ordered), so a launch cut short by a wait that
+// ran out cannot leave a later one with half-counted tickets.
 struct Scratch {
     uint64_t *partials = nullptr;
     uint32_t *tickets = nullptr;
@@ -2332,6 +2409,10 @@ int launch_stream(int dev, int sm_count, const uint16_t *logits, int64_t rows, i
             if (st != TF_TOPK_OK) return st;
             partials = s->partials;
             tickets = s->tickets;
+            // a launch whose wait ran out leaves its split rows' tickets half
+            // counted: start every launch from zero
+            const cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)ctas * sizeof(uint32_t), stream);
+            if (e != cudaSuccess) return fail_cuda(e);
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)ctas, 1, 1);
