@@ -309,3 +309,58 @@ def ranked_lists(rows: int, k: int, seed: int) -> tuple[np.ndarray, np.ndarray]:
         val[r, n - nan_tail: n] = _nan_bits(rng, nan_tail)
         count[r] = n
     return val, count
+
+
+# ----------------------------------------------------------------------------- draft head inputs
+
+@dataclass
+class HeadInputs:
+    """Inputs of the draft head that feeds the top-k: ``hidden`` [rows, dim]
+    and ``weight`` [vocab, dim], both uint16 bf16 bit patterns, plus k."""
+    name: str
+    hidden: np.ndarray
+    weight: np.ndarray
+    k: int
+
+    @property
+    def rows(self) -> int:
+        return self.hidden.shape[0]
+
+    @property
+    def dim(self) -> int:
+        return self.hidden.shape[1]
+
+    @property
+    def vocab(self) -> int:
+        return self.weight.shape[0]
+
+
+def head_inputs(rows: int, dim: int, vocab: int, k: int, seed: int) -> HeadInputs:
+    """Hidden states i/16 and weights j/64 with i, j uniform in -8..8.
+
+    Every value is a small integer over a power of two, so each product is a
+    multiple of 2^-10 and every partial sum of a dot product over dim <= 2^13
+    stays below 2^14 in magnitude: such sums are exact in fp32 and fp64 in
+    any order, and the bf16 logits they round to are unique.  Integers of at
+    most four significant bits make the bf16 values exact.  Rounded to bf16,
+    the logits collide often, so the top-k meets many ties.
+    """
+    rng = np.random.default_rng(seed)
+    hidden = round_to_bf16(rng.integers(-8, 9, size=(rows, dim)).astype(np.float32) / np.float32(16))
+    weight = np.empty((vocab, dim), np.uint16)
+    step = max(1, (1 << 24) // max(dim, 1))
+    for v0 in range(0, vocab, step):
+        v1 = min(vocab, v0 + step)
+        weight[v0:v1] = round_to_bf16(rng.integers(-8, 9, size=(v1 - v0, dim)).astype(np.float32) / np.float32(64))
+    return HeadInputs(f"head_{rows}x{dim}x{vocab}_k{k}", hidden, weight, k)
+
+
+def config_head_draft(seed: int = 5) -> HeadInputs:
+    """The draft head of the pages' workload: 15 rows x 98592 columns, k = 16,
+    from hidden states of 2048 dims (the pages do not give the drafter's width)."""
+    return head_inputs(15, 2048, 98592, 16, seed)
+
+
+def config_head_wide(seed: int = 6) -> HeadInputs:
+    """The 16 x 248320, k = 64 shape as a head (2048 dims)."""
+    return head_inputs(16, 2048, 248320, 64, seed)
