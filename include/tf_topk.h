@@ -39,6 +39,7 @@
 #ifndef TF_TOPK_H
 #define TF_TOPK_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -308,6 +309,51 @@ int32_t tf_topk_select_max_k(void); /* == TF_TOPK_MAX_K_WIDE */
  */
 int tf_topk_nucleus(const void *val, int32_t dtype, const int32_t *count, int64_t rows, int32_t k, float temperature,
                     float top_p, float *out_prob, int32_t *out_keep, void *stream);
+
+/*
+ * Draft head with the top-k in its epilogue (producer fusion).
+ *
+ * The operation is the one the top-k of TensorFold PR #713, change 3, is fed
+ * by: the drafter's head turns each draft position's hidden state into a row
+ * of bf16 logits (15 rows x 98592 columns there), and the top-k takes the
+ * best entries of each row.  The pages give the logits' shape and format
+ * only; the head is read here as the usual LM head, a matrix product with a
+ * [vocab][dim] weight, accumulated in fp32 and rounded to bf16 (round to
+ * nearest even).  This call computes that product and selects each row's
+ * top k from the rounded logits in the same kernel, so the logits never
+ * reach device memory:
+ *   logit[r][v] = bf16_rne( sum over d of hidden[r][d] * weight[v][d] )   (fp32 sum)
+ * and then exactly what tf_topk_bf16 gives for a [rows][vocab] logit matrix
+ * (same order, count, mask and empty slots).  The fp32 sum runs in the
+ * tensor cores' order: the result is bit-exact against any other
+ * implementation of the formula whenever that sum is exact in fp32 (as for
+ * small-integer products); otherwise the selection is exact over this
+ * kernel's own rounded logits.
+ *
+ *   hidden      device, bf16 [rows][dim], row stride dim; 16-byte aligned.
+ *   weight      device, bf16 [vocab][dim], row stride dim; 16-byte aligned.
+ *   rows        1..TF_TOPK_HEAD_MAX_ROWS (the draft window).
+ *   dim         >= 8, a multiple of 8 (16-byte rows).
+ *   vocab       1..2^31 - 64 columns of the logit rows.
+ *   k           1..TF_TOPK_MAX_K.
+ *   workspace   device, at least tf_topk_head_bf16_workspace(rows, k) bytes,
+ *               8-byte aligned, owned by the caller; its contents on entry do
+ *               not matter.  Calls that overlap on the GPU must not share it.
+ *   outputs     as for tf_topk_bf16 with cols = vocab.
+ * Asynchronous on `stream`; allocates nothing.  Returns a TF_TOPK_* status:
+ * ERR_SHAPE, ERR_K, ERR_NULL, ERR_ALIGN, ERR_SCRATCH (workspace too small),
+ * ERR_DEVICE or ERR_CUDA.
+ */
+#define TF_TOPK_HEAD_MAX_ROWS 16
+int tf_topk_head_bf16(const void *hidden, const void *weight, int32_t rows, int32_t dim, int64_t vocab, int32_t k,
+                      void *workspace, size_t workspace_bytes, int32_t *out_idx, uint16_t *out_val,
+                      int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream);
+
+/* Workspace bytes tf_topk_head_bf16 needs for (rows, k) on the current device
+ * (per CTA of its grid: for each row a k-entry list with a header word, a
+ * split ticket, and the fp32 partial sums of two tiles that a CTA may share
+ * with a neighbour); 0 for invalid arguments. */
+size_t tf_topk_head_bf16_workspace(int32_t rows, int32_t k);
 
 /* Human-readable text for a TF_TOPK_* status (static storage). */
 const char *tf_topk_strerror(int status);

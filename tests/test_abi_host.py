@@ -211,3 +211,23 @@ def test_nucleus_any_format_guards(lib):
     assert call(dtype=3) == topk.ERR_DTYPE and call(dtype=-1) == topk.ERR_DTYPE
     assert call(val=FAKE + 2) == topk.ERR_ALIGN and call(dtype=1, val=FAKE + 1) == topk.ERR_ALIGN
     assert call(k=65) == topk.ERR_K and call(rows=0) == topk.OK
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    ({"k": 0}, 3), ({"k": 65}, 3), ({"rows": 0}, 2), ({"rows": 17}, 2), ({"dim": 4}, 2), ({"dim": 12}, 2),
+    ({"vocab": 0}, 2), ({"hidden": 0}, 1), ({"workspace": 0}, 1), ({"weight": FAKE + 8}, 4),
+    ({"workspace": FAKE + 4}, 4), ({"val": FAKE + 1}, 4),
+])
+def test_head_guards_reject_before_any_cuda_work(lib, kwargs, status):
+    """tf_topk_head_bf16's argument checks run before the device is touched."""
+    a = {"hidden": FAKE, "weight": FAKE, "rows": 15, "dim": 2048, "vocab": 98592, "k": 16, "workspace": FAKE,
+         "idx": FAKE, "val": FAKE, "count": FAKE, "mask": FAKE}
+    a.update(kwargs)
+    assert lib.tf_topk_head_bf16(a["hidden"], a["weight"], a["rows"], a["dim"], a["vocab"], a["k"], a["workspace"],
+                                 1 << 30, a["idx"], a["val"], a["count"], a["mask"], None) == status
+
+
+def test_head_workspace_query_rejects_bad_arguments(lib):
+    assert lib.tf_topk_head_bf16_workspace(0, 16) == 0
+    assert lib.tf_topk_head_bf16_workspace(17, 16) == 0
+    assert lib.tf_topk_head_bf16_workspace(4, 65) == 0

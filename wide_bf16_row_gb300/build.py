@@ -13,7 +13,7 @@ from pathlib import Path
 
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
-SOURCES = [PKG / "csrc" / "tf_topk.cu"]
+SOURCES = [PKG / "csrc" / "tf_topk.cu", PKG / "csrc" / "tf_topk_head.cu"]
 HEADERS = [ROOT / "include" / "tf_topk.h"]
 LIBRARY = PKG / "libtf_topk.so"
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"

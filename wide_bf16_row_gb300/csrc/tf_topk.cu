@@ -2752,6 +2752,10 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
 
 } // namespace
 
+// Shared with the head entry points (a separate translation unit).
+int tf_topk_internal_fail_cuda(int cuda_error) { return fail_cuda(static_cast<cudaError_t>(cuda_error)); }
+uint32_t tf_topk_internal_head_fault_take();
+
 extern "C" {
 
 int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
@@ -2829,6 +2833,8 @@ int tf_topk_device_fault(void)
     uint32_t f = 0;
     cudaError_t e = cudaMemcpyFromSymbol(&f, g_fault, sizeof f);
     if (e != cudaSuccess) return -fail_cuda(e);
+    const uint32_t fh = tf_topk_internal_head_fault_take();
+    if (f == 0) f = fh;
     if (f != 0) {
         const uint32_t zero = 0;
         e = cudaMemcpyToSymbol(g_fault, &zero, sizeof zero);

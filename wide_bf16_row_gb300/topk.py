@@ -6,8 +6,9 @@ not been built, every entry point raises -- there is no fallback.
 
 Tensor-level calls: ``topk_bf16`` (bf16 rows, k <= 64, any launch plan),
 ``select_topk`` (bf16 / fp16 / fp32 rows, k <= 1024), ``merge_bf16``
-(per-shard lists into each row's top k) and ``nucleus_bf16`` (top-p
-probabilities over the lists).  The raw C entry points are exposed under
+(per-shard lists into each row's top k), ``nucleus_bf16`` (top-p
+probabilities over the lists) and ``head_topk_bf16`` (the draft head's
+product and the top-k in one kernel).  The raw C entry points are exposed under
 their C names.
 """
 from __future__ import annotations
@@ -78,6 +79,11 @@ def library() -> ctypes.CDLL:
                      "tf_topk_bf16_chunk_columns"):
             getattr(lib, name).restype = c_i32
             getattr(lib, name).argtypes = []
+        lib.tf_topk_head_bf16.restype = ctypes.c_int
+        lib.tf_topk_head_bf16.argtypes = [c_p, c_p, c_i32, c_i32, c_i64, c_i32, c_p, ctypes.c_size_t, c_p, c_p,
+                                          c_p, c_p, c_p]
+        lib.tf_topk_head_bf16_workspace.restype = ctypes.c_size_t
+        lib.tf_topk_head_bf16_workspace.argtypes = [c_i32, c_i32]
         lib.tf_topk_strerror.restype = ctypes.c_char_p
         lib.tf_topk_strerror.argtypes = [ctypes.c_int]
         lib.tf_topk_last_cuda_error.restype = ctypes.c_int
@@ -279,6 +285,63 @@ def select_topk(x, k: int, *, dtype: int | None = None, plan: int = 0, out=None,
     _check(tf_topk_select_with_plan(x.data_ptr(), dtype, rows, cols, row_stride, k, out[0].data_ptr(),
                                     out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(), plan,
                                     stream.cuda_stream))
+    return out
+
+
+HEAD_MAX_ROWS = 16
+
+
+def tf_topk_head_bf16(hidden: int, weight: int, rows: int, dim: int, vocab: int, k: int, workspace: int,
+                      workspace_bytes: int, out_idx: int, out_val: int, out_count: int, out_mask: int,
+                      stream: int | None) -> int:
+    """The fused draft-head entry point with raw pointers; returns the status code."""
+    return library().tf_topk_head_bf16(hidden, weight, rows, dim, vocab, k, workspace, workspace_bytes, out_idx,
+                                       out_val, out_count, out_mask, stream)
+
+
+def tf_topk_head_bf16_workspace(rows: int, k: int) -> int:
+    """Workspace bytes tf_topk_head_bf16 needs on the current device (0 for bad arguments)."""
+    return library().tf_topk_head_bf16_workspace(rows, k)
+
+
+def head_topk_bf16(hidden, weight, k: int, *, out=None, workspace=None, stream=None):
+    """Top-k of every row of the draft head's logits, bf16(hidden @ weight.T),
+    computed and selected in one kernel (the logits are never stored).
+
+    ``hidden``: CUDA bf16 (or int16 bits) [rows, dim], rows <= 16;
+    ``weight``: CUDA bf16 (or int16 bits) [vocab, dim]; both contiguous.
+    Returns ``(idx int32[rows,k], val bfloat16[rows,k], count int32[rows],
+    mask int32[rows])`` as ``topk_bf16`` gives them for the logit matrix.
+    ``workspace``: a CUDA uint8 tensor of at least
+    ``tf_topk_head_bf16_workspace(rows, k)`` bytes (allocated here if None).
+    """
+    import torch
+
+    for t in (hidden, weight):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError("hidden and weight must be contiguous 2-D CUDA tensors")
+        if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"expected bf16 bits, got {t.dtype}")
+    rows, dim = hidden.shape
+    vocab = weight.shape[0]
+    if weight.shape[1] != dim:
+        raise ValueError("hidden and weight disagree on dim")
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
+               torch.empty((rows, k), dtype=torch.bfloat16, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev),
+               torch.empty((rows,), dtype=torch.int32, device=dev))
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            need = tf_topk_head_bf16_workspace(rows, k) if 1 <= rows <= HEAD_MAX_ROWS else 0
+            workspace = torch.empty((max(need, 8),), dtype=torch.uint8, device=dev)
+        status = tf_topk_head_bf16(hidden.data_ptr(), weight.data_ptr(), rows, dim, vocab, k,
+                                   workspace.data_ptr(), workspace.numel(), out[0].data_ptr(), out[1].data_ptr(),
+                                   out[2].data_ptr(), out[3].data_ptr(), stream.cuda_stream)
+    _check(status)
     return out
 
 
