@@ -218,7 +218,7 @@ __device__ __forceinline__ uint64_t head_entry(uint32_t key, uint32_t col, uint3
     return ((uint64_t)key << 48) | ((uint64_t)(~col) << 16) | (uint64_t)bits;
 }
 
-// Entries of a descending list of distinct values that exceed x.
+// Entries of a non-increasing list that exceed x (a binary search).
 __device__ __forceinline__ int count_greater(const uint64_t *list, int len, uint64_t x)
 {
     int lo = 0, hi = len;
@@ -285,8 +285,18 @@ __device__ __forceinline__ bool epilogue_any(bool p)
 // Workspace of one call.  Lists: [rows][grid][k + 1] (a row's lists
 // contiguous for the merge).  Per boundary i between CTAs i - 1 and i that
 // cuts a tile: a ticket and the two fp32 partial sums of that tile.
+// Entries a list slot of the workspace holds: k rounded up to a power of
+// two, at least 2 (16-byte list blocks).
+__host__ __device__ __forceinline__ int list_stride(int k)
+{
+    int p = 2;
+    while (p < k) p <<= 1;
+    return p;
+}
+
 struct HeadWorkspace {
-    uint64_t *lists;
+    uint64_t *lists;    // [rows][grid][list_stride(k)], zero after a list's last entry
+    uint64_t *heads;    // [rows][grid]: length | flags << 32
     uint64_t *tickets;  // [grid]
     float *partials;    // [grid][2][kTileM][kRowsN]; part 0 from CTA i - 1, part 1 from CTA i
 };
@@ -573,19 +583,20 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                 epilogue_sync();
             }
         }
-        // this CTA's list per row into the workspace: [rows][grid][k + 1],
-        // a header (length | flags << 32) and the entries
+        // this CTA's list per row into the workspace: the entries, zero
+        // after the last, and a header (length | flags << 32)
 #pragma unroll
         for (int i = 0; i < kHalfRows; ++i) {
             const uint32_t f = __reduce_or_sync(0xFFFFFFFFu, (fl >> (3 * i)) & 7u);
             if (lane == 0 && f && r0 + i < rows) atomicOr(&sm.flags[r0 + i], f);
         }
         epilogue_sync();
+        const int P = list_stride(k);
         for (int r = ew; r < rows; r += kEpiWarps) {
-            uint64_t *out = ws.lists + ((size_t)r * grid + b) * (size_t)(k + 1);
+            uint64_t *out = ws.lists + ((size_t)r * grid + b) * (size_t)P;
             const int len = sm.run_len[r];
-            for (int j = lane; j < len; j += 32) out[1 + j] = sm.run[r][j];
-            if (lane == 0) out[0] = (uint64_t)(uint32_t)len | ((uint64_t)sm.flags[r] << 32);
+            for (int j = lane; j < P; j += 32) out[j] = j < len ? sm.run[r][j] : 0ull;
+            if (lane == 0) ws.heads[(size_t)r * grid + b] = (uint64_t)(uint32_t)len | ((uint64_t)sm.flags[r] << 32);
         }
     }
     grid_dependents_go(); // the merge may be scheduled; it still waits for this grid to finish
@@ -600,202 +611,201 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
 // ---------------------------------------------------------------- the merge of the per-CTA lists
 
 constexpr int kMergeThreads = 512;
+constexpr int kMergeWarps = kMergeThreads / 32;
+// The row's lists in shared memory; more than half of an SM's, so that merge
+// CTAs scheduled early (while the head kernel still runs) take an SM each.
+constexpr uint32_t kMergeSmemBytes = 120 * 1024;
+static_assert((size_t)kMaxGrid * kMaxK * sizeof(uint64_t) <= kMergeSmemBytes, "a row's lists fit");
 
-// One CTA per row merges the row's `lists` per-CTA lists: each holds its
-// CTA's best entries (descending, at most k), and the CTAs cover increasing
-// column ranges, so list order is column order.  The row's k-th key K* (the
-// k-th largest score, counted with multiplicity) comes from a radix select
-// over the keys, eight bits a pass.  The row is then every entry above K*
-// (fewer than k) and, of the entries at K*, the lowest columns: those of the
-// earliest lists first, each list's own in column order -- a scan over the
-// lists.  A CTA's list holds at most k entries, and a CTA never contributes
-// more than k to the row, so nothing the row needs was left out of a list.
-// One radix pass over the row's keys: a histogram of the digit (key >> shift)
-// & 0xFF over every entry (match: only entries whose high byte is match_hi).
-// Warp w takes lists w, w + warps, ...; a list's entries are sorted, so lanes
-// holding the same digit sit side by side: each run of equal digits adds its
-// length once, into the warp's own sub-histogram (hist_w: [warps][256]);
-// then the sub-histograms are summed into hist.  Block-uniform.
-__device__ __forceinline__ void merge_hist(const uint64_t *buf, int lists, int w, int k, int shift, uint32_t match_hi,
-                                           bool match, uint32_t *hist_w, uint32_t *hist)
+// One CTA per row merges the row's `lists` per-CTA lists.  A list holds its
+// CTA's best entries in descending order, then zeros, P entries in all (P =
+// k rounded up to a power of two, at least 2).  Entries are distinct (each
+// holds its column) and the entry order is the row order (score descending,
+// lower column first), so the row's top k are the k largest entries of the
+// union, and a zero (an empty slot) sorts below every entry.  The union's
+// top P comes from pairwise merges: for sorted A and B, max(A[i], B[P-1-i])
+// holds the top P of both and is bitonic, so half-cleaners sort it
+// (Batcher's bitonic merge).  A CTA never contributes more than k entries to
+// the row and its list keeps its best k, so nothing the row needs was left
+// out.
+//
+// A warp holds P-entry lists in registers: for P <= 32 a group of P lanes
+// holds one (entry i in lane i of the group, 32 / P groups side by side); for
+// P = 64 entry i sits in lane i % 32, register i / 32.
+
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m)
 {
-    constexpr int kWarps = kMergeThreads / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint32_t *mine = hist_w + warp * 256;
-    for (int i = lane; i < 256; i += 32) mine[i] = 0;
-    __syncwarp();
-    for (int j = warp; j < lists; j += kWarps) {
-        const uint64_t *lj = buf + (size_t)j * w;
-        const int n = (int)(uint32_t)lj[0];
-        for (int e0 = 0; e0 < n; e0 += 32) {
-            const int e = e0 + lane;
-            uint32_t digit = 0xFFFFFFFFu;
-            if (e < n) {
-                const uint32_t key = (uint32_t)(lj[1 + e] >> 48);
-                if (!match || (key >> 8) == match_hi) digit = (key >> shift) & 0xFFu;
-            }
-            const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, digit, 1);
-            const bool start = digit != 0xFFFFFFFFu && (lane == 0 || prev != digit);
-            const uint32_t starts = __ballot_sync(0xFFFFFFFFu, start);
-            const uint32_t valid = __ballot_sync(0xFFFFFFFFu, digit != 0xFFFFFFFFu);
-            if (start) {
-                // the run ends where the next run starts, or where the valid lanes end
-                const uint32_t later = starts & ~((2u << lane) - 1u);
-                const int end = later ? __ffs(later) - 1 : 32 - __clz(valid);
-                mine[digit] += (uint32_t)(end - lane);
-            }
-            __syncwarp();
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_idx64(uint64_t v, int src)
+{
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t min64(uint64_t a, uint64_t b) { return a > b ? b : a; }
+
+template <int P> struct MergeShape {
+    static constexpr int E = P > 32 ? 2 : 1;  // registers a lane holds per list
+    static constexpr int G = P > 32 ? 1 : 32 / P; // lists side by side in a warp
+};
+
+// N bitonic sequences of P entries each into descending order: half-cleaners
+// at distances P/2, .., 1; of each pair the lower index keeps the larger.
+template <int P, int N>
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t (&x)[N][MergeShape<P>::E], int lane)
+{
+    constexpr int E = MergeShape<P>::E;
+    if constexpr (P == 64) {
+#pragma unroll
+        for (int n = 0; n < N; ++n) {
+            const uint64_t hi = max64(x[n][0], x[n][1]), lo = min64(x[n][0], x[n][1]);
+            x[n][0] = hi;
+            x[n][1] = lo;
         }
     }
-    (void)k;
-    __syncthreads();
-    for (int i = tid; i < 256; i += kMergeThreads) {
-        uint32_t sum = 0;
 #pragma unroll
-        for (int x = 0; x < kWarps; ++x) sum += hist_w[x * 256 + i];
-        hist[i] = sum;
+    for (int d = (P > 32 ? 32 : P) / 2; d >= 1; d >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint64_t y = shfl_xor64(x[n][e], d);
+                x[n][e] = upper ? min64(x[n][e], y) : max64(x[n][e], y);
+            }
     }
 }
 
-// In one warp: the digit holding the need-th largest count of `hist`, and how
-// many lie in the digits above it.
-__device__ __forceinline__ void merge_pick(const uint32_t *hist, uint32_t need, uint32_t *digit, uint32_t *above)
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
 {
-    const int lane = threadIdx.x & 31;
-    uint32_t c8 = 0; // this lane's eight bins, from the top: 255 - 8 * lane ...
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c8 += hist[255 - 8 * lane - i];
-    uint32_t incl = c8;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += u;
-    }
-    const uint32_t excl = incl - c8;
-    if (excl < need && need <= incl) {
-        uint32_t a = excl;
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t bin = 255 - 8 * lane - i, h = hist[bin];
-            if (a + h >= need) {
-                *digit = bin;
-                *above = a;
-                break;
-            }
-            a += h;
-        }
-    }
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(saddr(dst)), "l"(src), "r"(bytes), "r"(saddr(bar))
+                 : "memory");
 }
 
-__global__ void __launch_bounds__(kMergeThreads)
-topk_head_merge_kernel(const uint64_t *__restrict__ ws_lists, int32_t lists, int32_t k,
-                       int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
+template <int P>
+__global__ void __launch_bounds__(kMergeThreads, 1)
+topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *__restrict__ ws_heads, int32_t lists,
+                       int32_t k, int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
                        int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
 {
-    grid_dependency_wait();
-    extern __shared__ __align__(16) uint64_t merge_dsmem[];
-    __shared__ uint32_t flags, entries, hist[256], digit_s, above_s;
-    __shared__ uint32_t hist_w[(kMergeThreads / 32) * 256];
-    __shared__ int32_t wsum[kMergeThreads / 32];
-    __shared__ uint64_t pick[kMaxK], fin[kMaxK];
+    constexpr int E = MergeShape<P>::E, G = MergeShape<P>::G;
+    extern __shared__ __align__(16) uint64_t merge_dsmem[]; // the row's lists: [lists][P]
+    __shared__ uint64_t part[2][kMergeWarps][P];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t flags;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
-    const int w = k + 1;
-    uint64_t *buf = merge_dsmem; // the row's lists, contiguous: [lists][k + 1] (header, entries)
+    const int g = P > 32 ? 0 : lane / P, i = P > 32 ? lane : lane % P; // lane group, entry
     if (tid == 0) {
+        mbar_init(&bar, 1);
         flags = 0;
-        entries = 0;
-    }
-    const uint64_t *src = ws_lists + (size_t)r * lists * w;
-    for (int i = tid; i < lists * w; i += kMergeThreads) buf[i] = __ldcg(src + i);
-    __syncthreads();
-    uint32_t my_flags = 0, my_n = 0;
-    for (int j = tid; j < lists; j += kMergeThreads) {
-        const uint64_t h = buf[(size_t)j * w];
-        my_flags |= (uint32_t)(h >> 32);
-        my_n += (uint32_t)h;
-    }
-    my_flags = __reduce_or_sync(0xFFFFFFFFu, my_flags);
-    my_n = __reduce_add_sync(0xFFFFFFFFu, my_n);
-    if (lane == 0) {
-        atomicOr(&flags, my_flags);
-        atomicAdd(&entries, my_n);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int total = (int)entries;
-    const int len = min(k, total);
-    // K*: with k or fewer entries every key is in; else two radix passes
-    uint32_t kstar = 0;
-    if (total > k) {
-        uint32_t need = (uint32_t)k, hi = 0;
-        for (int pass = 0; pass < 2; ++pass) {
-            merge_hist(buf, lists, w, k, pass == 0 ? 8 : 0, hi, pass == 1, hist_w, hist);
-            __syncthreads();
-            if (warp == 0) merge_pick(hist, need, &digit_s, &above_s);
-            __syncthreads();
-            if (pass == 0) hi = digit_s;
-            need -= above_s;
-        }
-        kstar = (hi << 8) | digit_s;
-    }
-    // per list: entries above K* (a prefix), then entries at K* (next); one
-    // scan over the lists (packed: above << 16 | ties) gives each its places
-    static_assert(kMaxGrid <= kMergeThreads, "one list per scanning thread");
-    uint32_t a = 0, tie = 0;
-    if (tid < lists) {
-        const uint64_t *lj = buf + (size_t)tid * w + 1;
-        const int n = (int)(uint32_t)buf[(size_t)tid * w];
-        if (total <= k) {
-            a = (uint32_t)n;
-        } else {
-            a = (uint32_t)count_greater(lj, n, ((uint64_t)(kstar + 1) << 48) - 1);
-            tie = (uint32_t)count_greater(lj, n, ((uint64_t)kstar << 48) - 1) - a;
-        }
-    }
-    const uint32_t mine = (a << 16) | tie;
-    uint32_t incl = mine;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += u;
-    }
-    if (lane == 31) wsum[warp] = (int32_t)incl;
-    __syncthreads();
-    uint32_t excl = incl - mine, all = 0;
-    for (int x = 0; x < kMergeThreads / 32; ++x) {
-        excl += x < warp ? (uint32_t)wsum[x] : 0u;
-        all += (uint32_t)wsum[x];
-    }
-    const uint32_t above_all = all >> 16;        // entries above K*: fewer than k
-    const uint32_t need = (uint32_t)len - above_all;
-    if (tid < lists) {
-        const uint64_t *lj = buf + (size_t)tid * w + 1;
-        const uint32_t a0 = excl >> 16, t0 = excl & 0xFFFFu;
-        for (uint32_t i = 0; i < a; ++i) pick[a0 + i] = lj[i];
-        for (uint32_t i = 0; i < tie && t0 + i < need; ++i) pick[above_all + t0 + i] = lj[a + i];
-    }
-    __syncthreads();
-    // the len chosen entries in order: a place is the number of larger ones
-    for (int t = tid; t < len; t += kMergeThreads) {
-        const uint64_t x = pick[t];
-        int rank = 0;
-        for (int u = 0; u < len; ++u) rank += pick[u] > x;
-        fin[rank] = x;
-    }
-    __syncthreads();
-    for (int t = tid; t < k; t += kMergeThreads) {
-        const int64_t o = (int64_t)r * k + t;
-        if (t < len) {
-            const uint64_t e = fin[t];
-            out_idx[o] = (int32_t)(~(uint32_t)(e >> 16));
-            out_val[o] = (uint16_t)(e & 0xFFFFu);
-        } else {
-            out_idx[o] = -1;
-            out_val[o] = 0x7FC0;
-        }
-    }
+    grid_dependency_wait();
     if (tid == 0) {
-        out_count[r] = len;
-        out_mask[r] = flags;
+        const uint32_t bytes = (uint32_t)lists * P * (uint32_t)sizeof(uint64_t);
+        mbar_expect_tx(&bar, bytes);
+        bulk_load(merge_dsmem, ws_entries + (size_t)r * lists * P, bytes, &bar);
+    }
+    uint32_t f = tid < lists ? (uint32_t)(__ldcg(ws_heads + (size_t)r * lists + tid) >> 32) : 0u;
+    if (__syncthreads_or(!mbar_wait(&bar, 0))) {
+        // the copy did not land in time: report, and wait (bounded) for it
+        // before the CTA's shared memory goes away
+        if (tid == 0) atomicCAS(&g_head_fault, 0u, kFaultWait);
+        mbar_wait(&bar, 0);
+        return;
+    }
+    // per lane group two running lists (two independent chains), starting
+    // empty; list j enters as max with its reverse, then a sort
+    uint64_t x[2][E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[0][e] = x[1][e] = 0;
+    const int nslots = kMergeWarps * G;
+#pragma unroll 1
+    for (int j0 = warp * G; j0 < lists; j0 += 2 * nslots) {
+        const int ja = j0 + g, jb = ja + nslots;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int ie = i + 32 * e;
+            const uint64_t ya = ja < lists ? merge_dsmem[(size_t)ja * P + (P - 1 - ie)] : 0ull;
+            const uint64_t yb = jb < lists ? merge_dsmem[(size_t)jb * P + (P - 1 - ie)] : 0ull;
+            x[0][e] = max64(x[0][e], ya);
+            x[1][e] = max64(x[1][e], yb);
+        }
+        bitonic_sort_desc<P, 2>(x, lane);
+    }
+    // the second chain reversed into the first, then the lane groups together
+    uint64_t a[1][E];
+    {
+        uint64_t c[E];
+        if constexpr (P == 64) {
+            c[0] = shfl_idx64(x[1][1], 31 - lane);
+            c[1] = shfl_idx64(x[1][0], 31 - lane);
+        } else {
+            c[0] = shfl_idx64(x[1][0], g * P + (P - 1 - i));
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) a[0][e] = max64(x[0][e], c[e]);
+        bitonic_sort_desc<P, 1>(a, lane);
+    }
+#pragma unroll
+    for (int h = 1; h < G; h <<= 1) {
+        const uint64_t c = shfl_idx64(a[0][0], (g ^ h) * P + (P - 1 - i));
+        a[0][0] = max64(a[0][0], c);
+        bitonic_sort_desc<P, 1>(a, lane);
+    }
+    f = __reduce_or_sync(0xFFFFFFFFu, f);
+    if (lane == 0 && f) atomicOr(&flags, f);
+    if (g == 0) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) part[0][warp][i + 32 * e] = a[0][e];
+    }
+    // a tree over the warps' lists: warp w merges lists 2w and 2w + 1
+    int src = 0;
+#pragma unroll 1
+    for (int n = kMergeWarps; n > 1; n >>= 1, src ^= 1) {
+        __syncthreads();
+        if (warp < n / 2) {
+            const uint64_t *A = part[src][2 * warp], *B = part[src][2 * warp + 1];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int ie = i + 32 * e;
+                a[0][e] = g == 0 ? max64(A[ie], B[P - 1 - ie]) : 0ull;
+            }
+            bitonic_sort_desc<P, 1>(a, lane);
+            if (n > 2 && g == 0) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) part[src ^ 1][warp][i + 32 * e] = a[0][e];
+            }
+        }
+    }
+    if (warp == 0) {
+        // the row: the first k entries; the empty ones (zero) come last
+        int len = 0;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int t = i + 32 * e;
+            const bool mine = g == 0 && t < k;
+            const bool full = mine && a[0][e] != 0;
+            len += __popc(__ballot_sync(0xFFFFFFFFu, full));
+            if (mine) {
+                const int64_t o = (int64_t)r * k + t;
+                out_idx[o] = full ? (int32_t)(~(uint32_t)(a[0][e] >> 16)) : -1;
+                out_val[o] = full ? (uint16_t)(a[0][e] & 0xFFFFu) : (uint16_t)0x7FC0;
+            }
+        }
+        if (lane == 0) {
+            out_count[r] = len;
+            out_mask[r] = flags;
+        }
     }
 }
 
@@ -803,10 +813,21 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_lists, int32_t lists, int
 
 constexpr size_t kHeadSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(HeadSmem);
 
-// The merge kernel's dynamic shared memory: the row's lists.
-size_t merge_smem_bytes(int lists, int k)
+
+
+// The merge kernel for each list stride P = 2, 4, .., 64.
+using MergeKernel = void (*)(const uint64_t *, const uint64_t *, int32_t, int32_t, int32_t *, uint16_t *, int32_t *,
+                             uint32_t *);
+constexpr int kMergeKernels = 6;
+const MergeKernel kMergeKernel[kMergeKernels] = {topk_head_merge_kernel<2>,  topk_head_merge_kernel<4>,
+                                                 topk_head_merge_kernel<8>,  topk_head_merge_kernel<16>,
+                                                 topk_head_merge_kernel<32>, topk_head_merge_kernel<64>};
+static_assert(kMaxK <= 64, "the largest list stride has a merge kernel");
+MergeKernel merge_kernel_for(int P)
 {
-    return (size_t)lists * (size_t)(k + 1) * sizeof(uint64_t); // the row's lists
+    int i = 0;
+    while ((2 << i) < P) ++i;
+    return kMergeKernel[i];
 }
 
 struct HeadDevice {
@@ -841,9 +862,9 @@ int head_setup(int *sm_count)
             } else {
                 e = cudaFuncSetAttribute(topk_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kHeadSmemBytes);
-                if (e == cudaSuccess)
-                    e = cudaFuncSetAttribute(topk_head_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)merge_smem_bytes(kMaxGrid, kMaxK));
+                for (int i = 0; i < kMergeKernels && e == cudaSuccess; ++i)
+                    e = cudaFuncSetAttribute(kMergeKernel[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kMergeSmemBytes);
                 if (e != cudaSuccess) return tf_topk_internal_fail_cuda((int)e);
                 if (!g_encode) {
                     void *fn = nullptr;
@@ -878,13 +899,14 @@ bool encode_map(CUtensorMap *map, const void *p, uint64_t inner, uint64_t outer,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Bytes of a call's workspace: the lists, the tickets, the partial sums (on a
-// 256-byte boundary, hence the slack).
+// Bytes of a call's workspace: the list entries and the partial sums, each
+// on a 256-byte boundary (vector loads and stores; hence the slack), the
+// list headers and the tickets.
 size_t workspace_bytes_for(int grid, int rows, int k)
 {
-    return (size_t)grid * ((size_t)rows * (size_t)(k + 1) * sizeof(uint64_t) + sizeof(uint64_t) +
+    return (size_t)grid * ((size_t)rows * (size_t)(list_stride(k) + 1) * sizeof(uint64_t) + sizeof(uint64_t) +
                            2 * (size_t)kTileM * kRowsN * sizeof(float)) +
-           256;
+           512;
 }
 
 // A call's epoch tags the tickets it takes, so a ticket an earlier call left
@@ -933,12 +955,14 @@ int run_head(const void *hidden, const void *weight, int32_t rows, int32_t dim, 
     cfg.stream = strm;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    uint64_t *lists = static_cast<uint64_t *>(workspace);
+    const auto align256 = [](const void *p) {
+        return reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(p) + 255) & ~(uintptr_t)255);
+    };
     HeadWorkspace ws;
-    ws.lists = lists;
-    ws.tickets = lists + (size_t)grid * rows * (k + 1);
-    // the partial sums start on a 256-byte boundary (vector stores)
-    ws.partials = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws.tickets + grid) + 255) & ~(uintptr_t)255);
+    ws.lists = static_cast<uint64_t *>(align256(workspace));
+    ws.heads = ws.lists + (size_t)rows * grid * list_stride(k);
+    ws.tickets = ws.heads + (size_t)rows * grid;
+    ws.partials = static_cast<float *>(align256(ws.tickets + grid));
 
     const uint64_t epoch = g_epoch.fetch_add(1, std::memory_order_relaxed) & (~0ull >> 2);
     cudaError_t e = cudaLaunchKernelEx(&cfg, topk_head_kernel, tw, th, rows, dim, vocab, k, ntiles, ws, epoch);
@@ -946,9 +970,9 @@ int run_head(const void *hidden, const void *weight, int32_t rows, int32_t dim, 
         cudaLaunchConfig_t mcfg = cfg;
         mcfg.gridDim = dim3((unsigned)rows, 1, 1);
         mcfg.blockDim = dim3(kMergeThreads, 1, 1);
-        mcfg.dynamicSmemBytes = merge_smem_bytes(grid, k);
-        e = cudaLaunchKernelEx(&mcfg, topk_head_merge_kernel, (const uint64_t *)lists, (int32_t)grid, k, out_idx,
-                               out_val, out_count, out_mask);
+        mcfg.dynamicSmemBytes = kMergeSmemBytes;
+        e = cudaLaunchKernelEx(&mcfg, merge_kernel_for(list_stride(k)), (const uint64_t *)ws.lists,
+                               (const uint64_t *)ws.heads, (int32_t)grid, k, out_idx, out_val, out_count, out_mask);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return tf_topk_internal_fail_cuda((int)e);
