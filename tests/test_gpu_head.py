@@ -63,6 +63,25 @@ def test_head_matches_the_oracle(rows, dim, vocab, k):
     assert topk.device_fault() == 0
 
 
+@pytest.mark.parametrize("vocab,k", [(98592, 16), (33000, 64), (200, 5)])
+def test_head_all_logits_tied(vocab, k):
+    """Every logit equal (one-hot hidden rows against a constant weight
+    column): each row is the first k columns, across tiles and CTAs that
+    select out of column order.  A row of zeros ties at +0."""
+    from wide_bf16_row_gb300 import topk
+
+    rows, dim = 4, 64
+    one = synth.round_to_bf16(np.array([1.0], np.float32))[0]
+    hidden = np.zeros((rows, dim), np.uint16)
+    hidden[:3, 5] = one                                   # rows 0-2: logit = weight[:, 5]; row 3 all zero
+    weight = np.zeros((vocab, dim), np.uint16)
+    weight[:, 5] = synth.round_to_bf16(np.array([0.75], np.float32))[0]
+    exp = head_oracle.topk(hidden, weight, k)
+    assert exp[0][0].tolist() == list(range(min(k, vocab))) + [-1] * (k - min(k, vocab))
+    got = _np(topk.head_topk_bf16(_dev(hidden), _dev(weight), k))
+    assert_same(got, exp, f"tied head {vocab} k={k}")
+
+
 def test_head_matches_cublas_then_topk():
     """cuBLAS's bf16 product (fp32 sum, rounded to bf16) followed by the
     ordinary top-k gives the same lists: the sums are exact."""

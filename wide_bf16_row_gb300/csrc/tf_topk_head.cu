@@ -28,10 +28,10 @@
 //              vocabulary column; two warps per 32 accumulator lanes, each
 //              taking half of the draft rows), round to bf16, and a running
 //              top-k per row: a value becomes a
-//              candidate only when it beats the row's running k-th (strictly:
-//              this CTA's tiles come in column order, so an equal value has
-//              the higher column and loses), and each row's candidates are
-//              merged into its list by one warp after every tile.
+//              candidate only when it beats the row's running k-th entry in
+//              the row's order (score, then the lower column), and each
+//              row's candidates are merged into its list by one warp after
+//              every tile.
 // At the end each CTA leaves one list per row in the caller's workspace.
 // topk_head_merge_kernel: one CTA per row merges those lists (the same order)
 // and writes the row.
@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -63,7 +64,7 @@ constexpr int kRowsN = 16;                    // draft rows, padded (MMA N)
 constexpr int kBoxK = 64;                     // dims per TMA box: one 128-byte swizzle row of bf16
 constexpr int kChunkK = 128;                  // dims per ring stage: two boxes side by side
 constexpr int kStages = 5;                    // TMA ring depth (180 KB in flight)
-constexpr int kHeadThreads = 320;             // producer warp, MMA warp, eight epilogue warps
+constexpr int kHeadThreads = 352;             // producer warp, MMA warp, eight epilogue warps, helper warp
 constexpr int kEpiThreads = 256;
 constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kHalfRows = kRowsN / 2;          // an epilogue warp's rows: one half of the draft rows
@@ -76,6 +77,8 @@ constexpr uint32_t kStageB = kBoxB * (kChunkK / kBoxK);  // 4 KB
 constexpr int kTmemCols = 2 * kRowsN;         // two fp32 accumulators of kRowsN columns
 constexpr uint32_t kHeadWaitLimit = 1u << 20;
 constexpr uint32_t kFaultWait = 1;
+constexpr uint64_t kAnyKey = 1ull << 32;      // (key << 32 | ~column) below every non-NaN key
+constexpr int kRankMerge = 16;                // candidates a row merges by ranks; more are sorted first
 constexpr int kMaxGrid = 160;                 // lists per row the merge kernel takes (GB300: 152 SMs)
 
 static_assert(TF_TOPK_HEAD_MAX_ROWS == kRowsN, "header and kernel agree on the draft rows");
@@ -90,18 +93,22 @@ struct __align__(16) HeadSmem {
     uint64_t run[kRowsN][kMaxK];              // running list per row (descending)
     uint64_t cand[kRowsN][kCandCap];          // this tile's candidates per row
     uint64_t tmp[kEpiWarps][kMaxK];           // per epilogue warp: merge output
-    uint32_t warp_bound[4][kRowsN];           // per lane group and row: a prefilter bound
     uint64_t full[kStages], empty[kStages];   // ring barriers
     uint64_t acc_full[2], acc_empty[2];       // accumulator barriers
     uint64_t drain;                           // the MMA warp's last products are done
     int32_t run_len[kRowsN];
     uint32_t cand_n[kRowsN];
-    uint32_t bound[kRowsN];                   // a candidate's canonical key must reach this
+    uint64_t bound[kRowsN];                   // a candidate's (key << 32 | ~column) must reach this
     uint32_t flags[kRowsN];
+    alignas(16) float cut_other[2][kTileM][kRowsN]; // the other part's partial sums of a cut tile this CTA finishes
+    uint64_t cut_ready[2];                    // epilogue -> helper: this part's partial sums are written
+    uint64_t cut_done[2];                     // helper -> epilogue: ticket taken (other part staged if last)
+    uint32_t cut_last[2];                     // this CTA arrived second at the cut tile's ticket
     uint32_t tmem_base;
     uint32_t abort;
-    uint32_t last;                            // the epilogue's view of a split tile's ticket
 };
+
+static_assert(offsetof(HeadSmem, cut_other) % 16 == 0, "the helper stages the other part's sums as float4");
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -134,6 +141,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
                      : "memory");
         if (ok) return true;
     }
+    return false;
+}
+
+// Whether the phase with this parity has completed (no wait).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(saddr(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// As mbar_wait, but also gives up once another warp has set *abort.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort)
+{
+    for (uint32_t i = 0; i < kHeadWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(ok)
+                     : "r"(saddr(bar)), "r"(parity)
+                     : "memory");
+        if (ok) return true;
+        if (*abort) return false;
+    }
+    atomicCAS(&g_head_fault, 0u, kFaultWait);
+    *abort = 1;
     return false;
 }
 
@@ -218,6 +255,23 @@ __device__ __forceinline__ uint64_t head_entry(uint32_t key, uint32_t col, uint3
     return ((uint64_t)key << 48) | ((uint64_t)(~col) << 16) | (uint64_t)bits;
 }
 
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m)
+{
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t shfl_idx64(uint64_t v, int src)
+{
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t min64(uint64_t a, uint64_t b) { return a > b ? b : a; }
+
 // Entries of a non-increasing list that exceed x (a binary search).
 __device__ __forceinline__ int count_greater(const uint64_t *list, int len, uint64_t x)
 {
@@ -232,39 +286,148 @@ __device__ __forceinline__ int count_greater(const uint64_t *list, int len, uint
     return lo;
 }
 
-// One row's candidates of this tile into its running list, by one warp: a
-// candidate's place is the candidates above it plus the running entries above
-// it; a running entry's, its index plus the candidates above it.
-__device__ __forceinline__ void merge_row(HeadSmem &sm, int r, int k, uint64_t *tmp)
+// A full bitonic sort into descending order of the 32 R entries a warp holds
+// (entry i in lane i % 32, register i / 32): merges of sorted runs of size 2,
+// 4, .., 32 R, each run ordered descending or ascending by its position, the
+// last one descending.
+// Compare-exchange: a gets the larger when desc, else the smaller.
+__device__ __forceinline__ void cx64(uint64_t &a, uint64_t &b, bool desc)
+{
+    const uint64_t hi = max64(a, b), lo = min64(a, b);
+    a = desc ? hi : lo;
+    b = desc ? lo : hi;
+}
+
+// A full bitonic sort into descending order of the 32 R entries a warp holds
+// (entry i in lane i % 32, register i / 32; R = 1, 2 or 4): merges of sorted
+// runs of size 2, 4, .., 32 R, each run ordered descending or ascending by
+// its position, the last one descending.  Stage loops stay rolled (the
+// epilogue's code must stay small: an instruction fetch that misses waits
+// behind the weight stream).
+template <int R>
+__device__ __forceinline__ void bitonic_full_sort(uint64_t (&x)[R], int lane)
+{
+    static_assert(R == 1 || R == 2 || R == 4, "one, two or four registers");
+#pragma unroll 1
+    for (int size = 2; size <= 32 * R; size <<= 1) {
+#pragma unroll 1
+        for (int d = size >> 1; d >= 1; d >>= 1) {
+            if (d == 64) { // registers e and e + 2, same lane
+                if constexpr (R == 4) {
+                    cx64(x[0], x[2], (0 & size) == 0);
+                    cx64(x[1], x[3], (32 & size) == 0);
+                }
+            } else if (d == 32) { // registers e and e + 1, same lane
+                if constexpr (R >= 2) {
+                    cx64(x[0], x[1], (0 & size) == 0);
+                    if constexpr (R == 4) cx64(x[2], x[3], (64 & size) == 0);
+                }
+            } else {
+                const bool lower = (lane & d) == 0;
+#pragma unroll
+                for (int e = 0; e < R; ++e) {
+                    const uint64_t y = shfl_xor64(x[e], d);
+                    const bool desc = ((e * 32 + lane) & size) == 0;
+                    x[e] = lower == desc ? max64(x[e], y) : min64(x[e], y);
+                }
+            }
+        }
+    }
+}
+
+// One row's candidates of this tile (n > a few) into its running list, by
+// one warp: the candidates sorted in registers, then the top P of them and
+// of the running list -- max(A[i], B[P - 1 - i]) over the sorted candidates
+// A and the running list B is bitonic and holds the top P of both (Batcher's
+// bitonic merge) -- sorted by half-cleaners.
+template <int R>
+__device__ __forceinline__ void merge_row_sorted(HeadSmem &sm, int r, int k, int P, int n, int rl)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t x[R];
+#pragma unroll
+    for (int e = 0; e < R; ++e) {
+        const int i = e * 32 + lane;
+        x[e] = i < n ? sm.cand[r][i] : 0ull;
+    }
+    bitonic_full_sort<R>(x, lane);
+    uint64_t y[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int i = e * 32 + lane, j = P - 1 - i;
+        const uint64_t a = e < R ? x[e < R ? e : 0] : 0ull;
+        const uint64_t bb = i < P && j < rl ? sm.run[r][j] : 0ull;
+        y[e] = i < P ? max64(a, bb) : 0ull;
+    }
+    if (P == 64) {
+        const uint64_t hi = max64(y[0], y[1]), lo = min64(y[0], y[1]);
+        y[0] = hi;
+        y[1] = lo;
+    }
+#pragma unroll 1
+    for (int d = (P < 32 ? P : 32) >> 1; d >= 1; d >>= 1) {
+        const bool lower = (lane & d) == 0;
+        const uint64_t z0 = shfl_xor64(y[0], d);
+        y[0] = lower ? max64(y[0], z0) : min64(y[0], z0);
+        if (P == 64) {
+            const uint64_t z1 = shfl_xor64(y[1], d);
+            y[1] = lower ? max64(y[1], z1) : min64(y[1], z1);
+        }
+    }
+    __syncwarp(); // every lane has read the old running list
+    const int len = min(k, rl + n);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int i = e * 32 + lane;
+        if (i < len) sm.run[r][i] = y[e];
+    }
+    __syncwarp();
+}
+
+// One row's candidates of this tile into its running list, by one warp.  A
+// few candidates: a candidate's place is the candidates above it plus the
+// running entries above it; a running entry's, its index plus the candidates
+// above it.  More: merge_row_sorted.  Then the new bound: once k entries are
+// in, a candidate must beat the k-th in the row's order.
+__device__ __forceinline__ void merge_row(HeadSmem &sm, int r, int k, int P, uint64_t *tmp)
 {
     const int lane = threadIdx.x & 31;
     const int n = (int)sm.cand_n[r];
     if (n == 0) return;
     const int rl = sm.run_len[r];
-    const uint64_t *c = sm.cand[r];
-    const uint64_t *run = sm.run[r];
-    for (int i = lane; i < n; i += 32) {
-        const uint64_t x = c[i];
-        int pos = count_greater(run, rl, x);
-        for (int j = 0; j < n; ++j) pos += c[j] > x;
-        if (pos < k) tmp[pos] = x;
+    if (n <= kRankMerge) {
+        const uint64_t *c = sm.cand[r];
+        const uint64_t *run = sm.run[r];
+        for (int i = lane; i < n; i += 32) {
+            const uint64_t x = c[i];
+            int pos = count_greater(run, rl, x);
+            for (int j = 0; j < n; ++j) pos += c[j] > x;
+            if (pos < k) tmp[pos] = x;
+        }
+        for (int j = lane; j < rl; j += 32) {
+            const uint64_t x = run[j];
+            int pos = j;
+            for (int i = 0; i < n; ++i) pos += c[i] > x;
+            if (pos < k) tmp[pos] = x;
+        }
+        __syncwarp();
+        const int len = min(k, rl + n);
+        for (int j = lane; j < len; j += 32) sm.run[r][j] = tmp[j];
+        __syncwarp();
+    } else if (n <= 32) {
+        merge_row_sorted<1>(sm, r, k, P, n, rl);
+    } else if (n <= 64) {
+        merge_row_sorted<2>(sm, r, k, P, n, rl);
+    } else {
+        merge_row_sorted<4>(sm, r, k, P, n, rl);
     }
-    for (int j = lane; j < rl; j += 32) {
-        const uint64_t x = run[j];
-        int pos = j;
-        for (int i = 0; i < n; ++i) pos += c[i] > x;
-        if (pos < k) tmp[pos] = x;
-    }
-    __syncwarp();
-    const int len = min(k, rl + n);
-    for (int j = lane; j < len; j += 32) sm.run[r][j] = tmp[j];
-    __syncwarp();
     if (lane == 0) {
+        const int len = min(k, rl + n);
         sm.run_len[r] = len;
         sm.cand_n[r] = 0;
-        // once k entries are in, a later column must beat the k-th strictly
-        sm.bound[r] = len == k ? (uint32_t)(sm.run[r][k - 1] >> 48) + 1u : 1u;
+        sm.bound[r] = len == k ? (sm.run[r][k - 1] >> 16) + 1u : kAnyKey;
     }
+    __syncwarp();
 }
 
 // True in every epilogue thread when `p` holds in any of them (a reduction on
@@ -301,44 +464,51 @@ struct HeadWorkspace {
     float *partials;    // [grid][2][kTileM][kRowsN]; part 0 from CTA i - 1, part 1 from CTA i
 };
 
-// Take the ticket of a split tile for this call: true for the second of its
-// two parts to arrive.  The word holds (call epoch << 2) | arrivals, so a word
-// an earlier call left counts as empty.  Release before, acquire after (the
-// partial sums written before the ticket are seen by the other part).
-__device__ __forceinline__ bool split_ticket_is_last(uint64_t *t, uint64_t epoch)
+// Arrive at a cut tile's ticket for this call: true for the part that
+// arrives second.  Both parts exchange the call's tag into the word; the
+// second finds the tag already there (a word an earlier call left holds
+// another tag).  Release and acquire at GPU scope: this CTA's partial sums,
+// written before (and ordered before this thread by the barrier it waited
+// on), are visible to the part that arrives second, and the other part's to
+// this thread when it arrives second.
+__device__ __forceinline__ bool take_split_ticket(uint64_t *t, uint64_t epoch)
 {
-    const uint64_t tag = epoch << 2;
-    __threadfence();
-    uint64_t cur = *reinterpret_cast<volatile uint64_t *>(t);
-    bool last = false;
-    for (int i = 0; i < 64; ++i) { // two arrivals per word: a few rounds at most
-        const uint64_t next = (cur & ~3ull) == tag ? cur + 1 : tag | 1ull;
-        const uint64_t seen = atomicCAS(reinterpret_cast<unsigned long long *>(t), cur, next);
-        if (seen == cur) {
-            last = (next & 3ull) == 2ull;
-            break;
-        }
-        cur = seen;
-    }
-    __threadfence();
-    return last;
+    const uint64_t tag = (epoch << 2) | 1ull;
+    uint64_t old;
+    asm volatile("atom.acq_rel.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(t), "l"(tag) : "memory");
+    return old == tag;
 }
 
 // The work of a call is the units (tile, K stage) in tile-major order, cut
 // into equal contiguous ranges, one per CTA (each at least a tile long, so a
 // tile falls in at most two CTAs).  A CTA's segments are its tiles, the first
 // and last possibly partial.  The two parts of a tile cut between CTAs i - 1
-// and i (the head at the end of i - 1, the tail at the start of i) each write
-// their partial sum and take the tile's ticket; the second to arrive adds the
-// other's partial to its own and selects the tile.  Nothing waits: usually
-// CTA i - 1 finishes the tile at its end; if CTA i arrives second it does so
-// at its start, before its own tiles.  Tiles reach the selection in column
-// order within a CTA either way.
+// and i (the head, in i - 1, and the tail, in i) each write their partial sum
+// and take the tile's ticket; the second to arrive adds the other's partial
+// to its own and selects the tile.  No part waits for the other.  A CTA
+// takes its cut segments first (the tail, then the head) and its full tiles
+// after them in column order.  The epilogue only writes a cut segment's
+// partial sums and keeps its own in registers; the CTA's helper warp takes
+// the ticket and, when this CTA is second, stages the other part's sums in
+// shared memory; the epilogue finishes such a tile after its first full
+// tile, by when the exchange has long completed.  Tiles thus reach the
+// selection out of column order; the running bound compares (score,
+// column), not the score alone.
 struct Segment {
     int64_t tile;
     int kc0, kc1;     // K stages [kc0, kc1) of the tile in this CTA
     bool tail, head;  // the tail (first segment) / head (last segment) of a cut tile
 };
+
+// The tile of a CTA's si-th segment in the order above.
+__device__ __forceinline__ int64_t segment_tile(int si, int64_t u0, int64_t u1, int nk)
+{
+    const int64_t t_first = u0 / nk, t_last = (u1 - 1) / nk;
+    const bool tail_cut = (u0 % nk) != 0, head_cut = (u1 % nk) != 0;
+    const int nc = (int)tail_cut + (int)head_cut;
+    if (si < nc) return tail_cut && si == 0 ? t_first : t_last;
+    return t_first + (tail_cut ? 1 : 0) + (si - nc);
+}
 
 __device__ __forceinline__ Segment segment_of(int64_t t, int64_t u0, int64_t u1, int nk)
 {
@@ -366,7 +536,7 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     const int nk = (dim + kChunkK - 1) / kChunkK;
     const int64_t units = ntiles * nk;
     const int64_t u0 = b * units / grid, u1 = (b + 1) * units / grid;
-    const int64_t t_first = u0 / nk, t_last = (u1 - 1) / nk;
+    const int nseg = (int)((u1 - 1) / nk - u0 / nk + 1); // segments of this CTA
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -378,13 +548,17 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
             mbar_init(&sm.acc_empty[i], kEpiThreads);
         }
         mbar_init(&sm.drain, 1);
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(&sm.cut_ready[c], kEpiThreads);
+            mbar_init(&sm.cut_done[c], 32);
+        }
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid < kRowsN) {
         sm.run_len[tid] = 0;
         sm.cand_n[tid] = 0;
-        sm.bound[tid] = 1;
+        sm.bound[tid] = kAnyKey;
         sm.flags[tid] = 0;
     }
     if (warp == 1) {
@@ -401,25 +575,28 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
 
     volatile uint32_t *abort = &sm.abort;
     if (warp == 0) {
-        // ---- TMA producer: the units [u0, u1) in order
+        // ---- TMA producer: the units of each segment, segments in order
         if (lane == 0) {
             uint32_t it = 0;
-            for (int64_t u = u0; u < u1 && !*abort; ++u, ++it) {
-                const int64_t t = u / nk;
-                const int kc = (int)(u - t * nk);
-                const uint32_t s = it % kStages, ph = it / kStages;
-                if (ph > 0 && !mbar_wait(&sm.empty[s], (ph - 1) & 1)) {
-                    atomicCAS(&g_head_fault, 0u, kFaultWait);
-                    *abort = 1;
-                    break;
-                }
-                mbar_expect_tx(&sm.full[s], kStageA + kStageB);
+            bool ok = true;
+            for (int si = 0; si < nseg && ok; ++si) {
+                const Segment g = segment_of(segment_tile(si, u0, u1, nk), u0, u1, nk);
+                for (int kc = g.kc0; kc < g.kc1; ++kc, ++it) {
+                    const uint32_t s = it % kStages, ph = it / kStages;
+                    if (*abort || (ph > 0 && !mbar_wait(&sm.empty[s], (ph - 1) & 1))) {
+                        if (!*abort) atomicCAS(&g_head_fault, 0u, kFaultWait);
+                        *abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&sm.full[s], kStageA + kStageB);
 #pragma unroll
-                for (int bx = 0; bx < kChunkK / kBoxK; ++bx) {
-                    const int32_t x = kc * kChunkK + bx * kBoxK;
-                    tma_load_2d(ring_a + (size_t)s * kStageA + bx * kBoxA, &tmap_w, x, (int32_t)(t * kTileM),
-                                &sm.full[s]);
-                    tma_load_2d(ring_b + (size_t)s * kStageB + bx * kBoxB, &tmap_h, x, 0, &sm.full[s]);
+                    for (int bx = 0; bx < kChunkK / kBoxK; ++bx) {
+                        const int32_t x = kc * kChunkK + bx * kBoxK;
+                        tma_load_2d(ring_a + (size_t)s * kStageA + bx * kBoxA, &tmap_w, x,
+                                    (int32_t)(g.tile * kTileM), &sm.full[s]);
+                        tma_load_2d(ring_b + (size_t)s * kStageB + bx * kBoxB, &tmap_h, x, 0, &sm.full[s]);
+                    }
                 }
             }
             // the copies issued land before the CTA leaves: each stage's last
@@ -434,9 +611,8 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
-            int si = 0;
-            for (int64_t t = t_first; t <= t_last && ok && !*abort; ++t, ++si) {
-                const Segment g = segment_of(t, u0, u1, nk);
+            for (int si = 0; si < nseg && ok && !*abort; ++si) {
+                const Segment g = segment_of(segment_tile(si, u0, u1, nk), u0, u1, nk);
                 const uint32_t buf = si & 1, uu = si >> 1;
                 if (uu > 0 && !mbar_wait(&sm.acc_empty[buf], (uu - 1) & 1)) {
                     ok = false;
@@ -473,7 +649,7 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0);
         }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // ---- epilogue: warps 2..9.  Warp w reads accumulator lanes 32 * (w % 4) ..
         // (the tile rows = vocabulary columns of its threads) and one half of
         // the draft rows: rows 8 h .. 8 h + 7, h = (w - 2) / 4.
@@ -482,47 +658,11 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
         const int h = ew >> 2;
         const int r0 = h * kHalfRows;
         const int trow = 32 * q + lane; // this thread's row of the tile
+        const int P = list_stride(k);   // the running lists' merge width
         uint32_t fl = 0;                // non-finite flags, 3 bits per row of the half
-        int si = 0;
-        for (int64_t t = t_first; t <= t_last; ++t, ++si) {
-            const Segment g = segment_of(t, u0, u1, nk);
-            const uint32_t buf = si & 1, uu = si >> 1;
-            const bool ok = mbar_wait(&sm.acc_full[buf], uu & 1);
-            if (epilogue_any(!ok || *abort)) {
-                if (!ok) atomicCAS(&g_head_fault, 0u, kFaultWait);
-                *abort = 1;
-                break;
-            }
-            tc_fence_after();
-            uint32_t acc[kHalfRows];
-            tmem_load8(tmem + buf * kRowsN + r0 + ((uint32_t)(32 * q) << 16), acc);
-            tc_fence_before();
-            mbar_arrive(&sm.acc_empty[buf]); // the accumulator may take the next segment's products
-            if (g.tail || g.head) {
-                // a cut tile: hand this part's sum over; the second part in finishes it
-                const int64_t bnd = g.tail ? b : b + 1;
-                float4 *mine = reinterpret_cast<float4 *>(
-                    ws.partials + (((size_t)bnd * 2 + (g.tail ? 1 : 0)) * kTileM + trow) * kRowsN + r0);
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    mine[j] = make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
-                                          __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
-                __threadfence();
-                epilogue_sync();
-                if (ew == 0 && lane == 0) sm.last = split_ticket_is_last(&ws.tickets[bnd], epoch) ? 1u : 0u;
-                epilogue_sync();
-                if (!sm.last) continue;
-                const float4 *other = reinterpret_cast<const float4 *>(
-                    ws.partials + (((size_t)bnd * 2 + (g.tail ? 0 : 1)) * kTileM + trow) * kRowsN + r0);
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const float4 p = __ldcg(other + j);
-                    acc[4 * j] = __float_as_uint(__uint_as_float(acc[4 * j]) + p.x);
-                    acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + p.y);
-                    acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + p.z);
-                    acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + p.w);
-                }
-            }
+        // the selection of one tile's sums (fp32 bits, rows r0 .. r0 + 7 of
+        // this thread's column); block-uniform (epilogue barriers inside)
+        auto select_tile = [&](const uint32_t (&acc)[kHalfRows], int64_t t) {
             const int64_t v = t * kTileM + trow;
             const bool in_vocab = v < vocab;
             uint32_t keys[kHalfRows], bits16[kHalfRows];
@@ -533,55 +673,95 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                 keys[i] = live ? canon_key(bits16[i]) : 0u;
                 if (live) fl |= nonfinite_flag(bits16[i]) << (3 * i);
             }
-            // rows whose list is not full yet (a CTA's first tile): a prefilter
-            // bound for the tile -- each lane group's j-th largest key, j =
-            // ceil(k / 4); the smallest of the four is reached by at least k
-            // keys of the tile
-            bool prefilter = false;
-#pragma unroll
-            for (int r = 0; r < kRowsN; ++r) prefilter |= r < rows && sm.run_len[r] < k;
-            if (prefilter) { // block-uniform: run_len changes only between barriers
-                const int j = (k + 3) / 4;
-#pragma unroll
-                for (int i = 0; i < kHalfRows; ++i) {
-                    const int r = r0 + i;
-                    if (r < rows && sm.run_len[r] < k) {
-                        uint32_t x = keys[i], cnt = 0, tw = 0;
-                        for (int it = 0; it < j; ++it) {
-                            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, x);
-                            if (m == 0) break;
-                            cnt += __popc(__ballot_sync(0xFFFFFFFFu, x == m));
-                            if (cnt >= (uint32_t)j) {
-                                tw = m;
-                                break;
-                            }
-                            if (x == m) x = 0;
-                        }
-                        if (lane == 0) sm.warp_bound[q][r] = tw;
-                    }
-                }
-                epilogue_sync();
-            }
+            // a value becomes a candidate when it beats the row's bound; a
+            // warp takes its slots in a row's candidates with one atomic
             bool pushed = false;
 #pragma unroll
             for (int i = 0; i < kHalfRows; ++i) {
                 const int r = r0 + i;
-                if (r < rows && keys[i] != 0) {
-                    uint32_t bound = sm.bound[r];
-                    if (sm.run_len[r] < k)
-                        bound = max(bound, min(min(sm.warp_bound[0][r], sm.warp_bound[1][r]),
-                                               min(sm.warp_bound[2][r], sm.warp_bound[3][r])));
-                    if (keys[i] >= bound) {
-                        const uint32_t slot = atomicAdd(&sm.cand_n[r], 1u);
-                        sm.cand[r][slot] = head_entry(keys[i], (uint32_t)v, bits16[i]);
-                        pushed = true;
-                    }
-                }
+                if (r >= rows) break; // warp-uniform
+                const bool want =
+                    keys[i] != 0 && ((((uint64_t)keys[i] << 32) | (uint32_t)~(uint32_t)v) >= sm.bound[r]);
+                const uint32_t m = __ballot_sync(0xFFFFFFFFu, want);
+                if (m == 0) continue;
+                const int leader = __ffs(m) - 1;
+                uint32_t base = 0;
+                if (lane == leader) base = atomicAdd(&sm.cand_n[r], (uint32_t)__popc(m));
+                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                if (want) sm.cand[r][base + __popc(m & ((1u << lane) - 1u))] = head_entry(keys[i], (uint32_t)v, bits16[i]);
+                pushed = true;
             }
             if (epilogue_any(pushed)) { // a barrier too: the candidates are in
-                for (int r = ew; r < rows; r += kEpiWarps) merge_row(sm, r, k, sm.tmp[ew]);
+#pragma unroll 1
+                for (int r = ew; r < rows; r += kEpiWarps) merge_row(sm, r, k, P, sm.tmp[ew]);
                 epilogue_sync();
             }
+        };
+        // The CTA's cut segments are its first nc; their own sums wait in
+        // registers until the helper has taken the tickets.  After each full
+        // tile the epilogue selects the cut tiles whose exchange is done (the
+        // test does not wait: a global round trip under the weight stream
+        // takes microseconds) and it finishes as first part; at the end it
+        // waits for the rest.  One loop, one selection site.
+        const int nc = (int)((u0 % nk) != 0) + (int)((u1 % nk) != 0);
+        uint32_t cut_acc0[kHalfRows], cut_acc1[kHalfRows];
+        int cuts_next = 0; // cut segments [0, cuts_next) are done with
+        int si = 0;        // next segment to read from TMEM
+        while (true) {
+            uint32_t acc[kHalfRows];
+            int64_t t = -1;
+            if (cuts_next < nc && si >= nc &&
+                (si >= nseg || epilogue_any(mbar_test(&sm.cut_done[cuts_next], 0)))) {
+                const int c = cuts_next++;
+                const bool ok = mbar_wait(&sm.cut_done[c], 0);
+                if (epilogue_any(!ok || *abort)) {
+                    if (!ok) atomicCAS(&g_head_fault, 0u, kFaultWait);
+                    *abort = 1;
+                    break;
+                }
+                if (!sm.cut_last[c]) continue; // the other part finishes the tile
+#pragma unroll
+                for (int i = 0; i < kHalfRows; ++i)
+                    acc[i] = __float_as_uint(__uint_as_float(c == 0 ? cut_acc0[i] : cut_acc1[i]) +
+                                             sm.cut_other[c][trow][r0 + i]);
+                t = segment_tile(c, u0, u1, nk);
+            } else {
+                if (si >= nseg) break;
+                const Segment g = segment_of(segment_tile(si, u0, u1, nk), u0, u1, nk);
+                const uint32_t buf = si & 1, uu = si >> 1;
+                const bool ok = mbar_wait(&sm.acc_full[buf], uu & 1);
+                if (epilogue_any(!ok || *abort)) {
+                    if (!ok) atomicCAS(&g_head_fault, 0u, kFaultWait);
+                    *abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                tmem_load8(tmem + buf * kRowsN + r0 + ((uint32_t)(32 * q) << 16), acc);
+                tc_fence_before();
+                mbar_arrive(&sm.acc_empty[buf]); // the accumulator may take the next segment's products
+                if (g.tail || g.head) {
+                    // a cut tile (si < nc): this part's sums to the workspace
+                    // for the other part, and kept for finishing it here
+                    const int64_t bnd = g.tail ? b : b + 1;
+                    float4 *mine = reinterpret_cast<float4 *>(
+                        ws.partials + (((size_t)bnd * 2 + (g.tail ? 1 : 0)) * kTileM + trow) * kRowsN + r0);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        mine[j] = make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                                              __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3]));
+#pragma unroll
+                    for (int i = 0; i < kHalfRows; ++i) {
+                        if (si == 0) cut_acc0[i] = acc[i];
+                        else cut_acc1[i] = acc[i];
+                    }
+                    mbar_arrive(&sm.cut_ready[si]);
+                    ++si;
+                    continue;
+                }
+                t = g.tile;
+                ++si;
+            }
+            select_tile(acc, t);
         }
         // this CTA's list per row into the workspace: the entries, zero
         // after the last, and a header (length | flags << 32)
@@ -591,12 +771,33 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
             if (lane == 0 && f && r0 + i < rows) atomicOr(&sm.flags[r0 + i], f);
         }
         epilogue_sync();
-        const int P = list_stride(k);
         for (int r = ew; r < rows; r += kEpiWarps) {
             uint64_t *out = ws.lists + ((size_t)r * grid + b) * (size_t)P;
             const int len = sm.run_len[r];
             for (int j = lane; j < P; j += 32) out[j] = j < len ? sm.run[r][j] : 0ull;
             if (lane == 0) ws.heads[(size_t)r * grid + b] = (uint64_t)(uint32_t)len | ((uint64_t)sm.flags[r] << 32);
+        }
+    } else {
+        // ---- helper (warp 2 + kEpiWarps): the tickets of the cut tiles, in
+        // the epilogue's order; when this CTA arrives second it stages the
+        // other part's partial sums for the epilogue
+        const int nc = (int)((u0 % nk) != 0) + (int)((u1 % nk) != 0);
+        for (int c = 0; c < nc; ++c) {
+            const Segment g = segment_of(segment_tile(c, u0, u1, nk), u0, u1, nk);
+            const int64_t bnd = g.tail ? b : b + 1;
+            if (!mbar_wait_or_abort(&sm.cut_ready[c], 0, abort)) break;
+            uint32_t last = 0;
+            if (lane == 0) last = take_split_ticket(&ws.tickets[bnd], epoch) ? 1u : 0u;
+            __syncwarp(); // the other lanes' reads below come after lane 0's acquire
+            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+            if (last) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    ws.partials + ((size_t)bnd * 2 + (g.tail ? 0 : 1)) * kTileM * kRowsN);
+                float4 *dst = reinterpret_cast<float4 *>(&sm.cut_other[c][0][0]);
+                for (int i = lane; i < kTileM * kRowsN / 4; i += 32) dst[i] = __ldcg(src + i);
+            }
+            if (lane == 0) sm.cut_last[c] = last;
+            mbar_arrive(&sm.cut_done[c]);
         }
     }
     grid_dependents_go(); // the merge may be scheduled; it still waits for this grid to finish
@@ -632,23 +833,6 @@ static_assert((size_t)kMaxGrid * kMaxK * sizeof(uint64_t) <= kMergeSmemBytes, "a
 // A warp holds P-entry lists in registers: for P <= 32 a group of P lanes
 // holds one (entry i in lane i of the group, 32 / P groups side by side); for
 // P = 64 entry i sits in lane i % 32, register i / 32.
-
-__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m)
-{
-    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
-    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-__device__ __forceinline__ uint64_t shfl_idx64(uint64_t v, int src)
-{
-    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
-    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
-__device__ __forceinline__ uint64_t min64(uint64_t a, uint64_t b) { return a > b ? b : a; }
 
 template <int P> struct MergeShape {
     static constexpr int E = P > 32 ? 2 : 1;  // registers a lane holds per list
@@ -812,6 +996,7 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
 // ---------------------------------------------------------------- host side
 
 constexpr size_t kHeadSmemBytes = 1024 + (size_t)kStages * (kStageA + kStageB) + sizeof(HeadSmem);
+static_assert(kHeadSmemBytes <= 227 * 1024, "the head kernel's shared memory fits one CTA");
 
 
 
