@@ -527,7 +527,9 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                  uint64_t epoch)
 {
     extern __shared__ __align__(1024) uint8_t head_dsmem[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(head_dsmem) + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned (the swizzled tiles); offset from the shared array
+    // itself, so that every access below stays a shared-memory access
+    uint8_t *base = head_dsmem + ((1024u - (saddr(head_dsmem) & 1023u)) & 1023u);
     uint8_t *ring_a = base;                                 // kStages x kStageA
     uint8_t *ring_b = base + (size_t)kStages * kStageA;     // kStages x kStageB
     HeadSmem &sm = *reinterpret_cast<HeadSmem *>(ring_b + (size_t)kStages * kStageB);
