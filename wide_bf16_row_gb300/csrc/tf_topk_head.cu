@@ -676,21 +676,30 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
                 if (live) fl |= nonfinite_flag(bits16[i]) << (3 * i);
             }
             // a value becomes a candidate when it beats the row's bound; a
-            // warp takes its slots in a row's candidates with one atomic
-            bool pushed = false;
+            // warp takes its slots in a row's candidates with one atomic.
+            // Three passes over the rows, so that their loads, ballots and
+            // atomics overlap.
+            bool want[kHalfRows];
+            uint32_t m[kHalfRows], base[kHalfRows];
 #pragma unroll
             for (int i = 0; i < kHalfRows; ++i) {
                 const int r = r0 + i;
-                if (r >= rows) break; // warp-uniform
-                const bool want =
-                    keys[i] != 0 && ((((uint64_t)keys[i] << 32) | (uint32_t)~(uint32_t)v) >= sm.bound[r]);
-                const uint32_t m = __ballot_sync(0xFFFFFFFFu, want);
-                if (m == 0) continue;
-                const int leader = __ffs(m) - 1;
-                uint32_t base = 0;
-                if (lane == leader) base = atomicAdd(&sm.cand_n[r], (uint32_t)__popc(m));
-                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                if (want) sm.cand[r][base + __popc(m & ((1u << lane) - 1u))] = head_entry(keys[i], (uint32_t)v, bits16[i]);
+                want[i] = r < rows && keys[i] != 0 &&
+                          ((((uint64_t)keys[i] << 32) | (uint32_t)~(uint32_t)v) >= sm.bound[r < rows ? r : 0]);
+                m[i] = __ballot_sync(0xFFFFFFFFu, want[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < kHalfRows; ++i) {
+                base[i] = 0;
+                if (m[i] != 0 && lane == __ffs(m[i]) - 1) base[i] = atomicAdd(&sm.cand_n[r0 + i], (uint32_t)__popc(m[i]));
+            }
+            bool pushed = false;
+            const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+            for (int i = 0; i < kHalfRows; ++i) {
+                if (m[i] == 0) continue; // warp-uniform
+                const uint32_t at = __shfl_sync(0xFFFFFFFFu, base[i], __ffs(m[i]) - 1) + __popc(m[i] & below);
+                if (want[i]) sm.cand[r0 + i][at] = head_entry(keys[i], (uint32_t)v, bits16[i]);
                 pushed = true;
             }
             if (epilogue_any(pushed)) { // a barrier too: the candidates are in
