@@ -363,6 +363,102 @@ def per_config_table(dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:
     return table
 
 
+# The draft heads the fused head-with-top-k entry point is measured on.
+HEAD_CONFIGS = (
+    ("15x2048x98592_k16", "config_head_draft"),
+    ("16x2048x248320_k64", "config_head_wide"),
+)
+
+
+def measure_head(h, dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:
+    """One draft head through tf_topk_head_bf16 (the product and the top-k in
+    one kernel, plus the merge of the per-CTA lists) and, on the same device,
+    the two-step path it replaces: cuBLAS's bf16 product into a logit matrix,
+    then tf_topk_bf16.  Each timed as a CUDA graph of back-to-back calls
+    (the weight matrix exceeds L2, so every call streams it from HBM)."""
+    import torch
+
+    from wide_bf16_row_gb300 import topk
+
+    rows, dim, vocab, k = h.hidden.shape[0], h.hidden.shape[1], h.weight.shape[0], h.k
+    hid = torch.from_numpy(h.hidden.view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(h.weight.view(np.int16)).to(dev).view(torch.bfloat16)
+    ws = torch.empty((topk.tf_topk_head_bf16_workspace(rows, k),), dtype=torch.uint8, device=dev)
+    out = (torch.empty((rows, k), dtype=torch.int32, device=dev),
+           torch.empty((rows, k), dtype=torch.int16, device=dev),
+           torch.empty((rows,), dtype=torch.int32, device=dev),
+           torch.empty((rows,), dtype=torch.int32, device=dev))
+    out2 = tuple(torch.empty_like(t) for t in out)
+    logits = torch.empty((rows, vocab), dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream(dev)
+
+    def fused():
+        topk.head_topk_bf16(hid, w, k, out=out, workspace=ws, stream=side)
+
+    def two_step():
+        torch.matmul(hid, w.t(), out=logits)
+        topk.topk_bf16(logits, k, out=out2, stream=side)
+
+    def graph_us(fn, n_calls=20, reps=20):
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(n_calls):
+                fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            a.record(side)
+            for _ in range(reps):
+                graph.replay()
+            b.record(side)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e3 / (reps * n_calls)
+
+    us_fused = graph_us(fused)
+    us_two = graph_us(two_step)
+    same = all(bool(torch.equal(x, y)) for x, y in zip(out, out2))
+    alg = vocab * dim * 2 + rows * dim * 2 + rows * k * 6 + rows * 8
+    gbs = alg / (us_fused * 1e-6) / 1e9
+    res = {
+        "rows": rows, "dim": dim, "vocab": vocab, "k": k,
+        "us_per_call": us_fused,
+        "us_per_call_cublas_then_topk": us_two,
+        "speedup_vs_cublas_then_topk": us_two / us_fused,
+        "rows_per_s": rows / (us_fused * 1e-6),
+        "gbs": gbs, "frac_of_peak": gbs / peak, "bound": "hbm",
+        "algorithmic_bytes": alg,
+        "same_result_as_cublas_then_topk": same,
+        "timing": "CUDA graph of 20 back-to-back calls, 20 replays, CUDA events; weight > L2",
+    }
+    if cpu:
+        from oracle import head as head_oracle
+
+        n = 1
+        head_oracle.topk(h.hidden[:n], h.weight, k)  # warm
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            head_oracle.topk(h.hidden[:n], h.weight, k)
+            reps += 1
+            if time.perf_counter() - t0 > cpu_seconds / 2:
+                break
+        res["oracle_rows_per_s"] = reps * n / (time.perf_counter() - t0)
+        res["oracle_sample"] = f"{n} row(s) of the head per call, numpy float64 product on the host's BLAS threads"
+    del hid, w, ws, logits
+    torch.cuda.empty_cache()
+    return res
+
+
+def head_table(dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:
+    from wide_bf16_row_gb300 import synth
+
+    return {name: measure_head(getattr(synth, fn)(), dev, peak, cpu, cpu_seconds) for name, fn in HEAD_CONFIGS}
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 def time_oracle(w, budget_s: float, rows_per_call: int | None = None, bits: np.ndarray | None = None,
@@ -478,10 +574,11 @@ def run_ours(args) -> None:
     label = run_label(w, fmt, k)
 
     def call(view):
+        s = torch.cuda.current_stream(dev)  # the capture stream while a graph is captured
         if fmt == "bf16" and k == w.k and plan_arg != 64:
-            topk.topk_bf16(view, k, plan=plan_arg, out=out, stream=stream)
+            topk.topk_bf16(view, k, plan=plan_arg, out=out, stream=s)
         else:
-            topk.select_topk(view, k, dtype=code, plan=plan_arg, out=out, stream=stream)
+            topk.select_topk(view, k, dtype=code, plan=plan_arg, out=out, stream=s)
 
     def step(i: int):
         call(views[i % nbuf])
@@ -489,6 +586,32 @@ def run_ours(args) -> None:
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
+    # the K timed steps, captured once as a CUDA graph (the same launches on
+    # the same rotating inputs), so that the timed region holds device work
+    # only, not the host's issue of each launch
+    graph, inner = None, None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.stream(cap):  # any per-stream scratch is made before the capture
+            step(0)
+        torch.cuda.synchronize(dev)
+        # events recorded by the graph itself, around its K launches: no
+        # host issue gap between the start event and the first launch
+        try:
+            inner = (torch.cuda.Event(enable_timing=True, external=True),
+                     torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            inner = None
+        with torch.cuda.graph(graph, stream=cap):
+            if inner:
+                inner[0].record(cap)
+            for i in range(args.steps):
+                step(i)
+            if inner:
+                inner[1].record(cap)
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize(dev)
 
     # the timed launches run back to back (each may be scheduled while the
     # previous one finishes); isolated launches are timed afterwards, apart
@@ -501,8 +624,11 @@ def run_ours(args) -> None:
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     start.record(stream)
-    for i in range(args.steps):
-        step(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
@@ -511,7 +637,8 @@ def run_ours(args) -> None:
     clocks = sampler.summary(t0, t1) if sampler else None
     if sampler:
         sampler.stop()
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_outer_ms = start.elapsed_time(end)
+    elapsed_ms = inner[0].elapsed_time(inner[1]) if graph is not None and inner else elapsed_outer_ms
     launch_ms = isolated_launches(step, stream, dev, n=min(50, max(3, args.steps)))
 
     # L2-warm: the same input every call (draft logits often sit in L2 right
@@ -569,8 +696,10 @@ def run_ours(args) -> None:
     d2h = rows * k * 4 + rows * k * esize + rows * 4 + rows * 4
 
     per_config = None
+    head = None
     if rank == 0 and world == 1 and not args.no_per_config:
         per_config = per_config_table(dev, peak, not args.no_cpu_baseline, min(0.6, args.cpu_seconds))
+        head = head_table(dev, peak, not args.no_cpu_baseline, min(0.6, args.cpu_seconds))
 
     cpu = None
     cpu_1core = None
@@ -609,7 +738,13 @@ def run_ours(args) -> None:
                          "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "launches_timed": args.steps,
-                         "duration": "CUDA events around all timed launches, back to back, / launches"},
+                         "duration": ("CUDA events around all timed launches, back to back "
+                                      + ("(replayed from a CUDA graph that records the events itself)"
+                                         if graph is not None and inner else
+                                         "(replayed from a CUDA graph)" if graph is not None else
+                                         "(issued from Python)")
+                                      + ", / launches"),
+                         "ms_per_step_host_events": elapsed_outer_ms / args.steps},
             "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": args.steps,
@@ -617,6 +752,7 @@ def run_ours(args) -> None:
             "cpu_baseline": cpu,
             "cpu_baseline_1core": cpu_1core,
             "per_config": per_config,
+            "head": head,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -639,6 +775,8 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="issue the timed launches one by one from Python instead of replaying them as a CUDA graph")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload table (every named workload and sweep points)")
     args = ap.parse_args(argv)

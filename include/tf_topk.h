@@ -339,6 +339,8 @@ int tf_topk_nucleus(const void *val, int32_t dtype, const int32_t *count, int64_
  *   workspace   device, at least tf_topk_head_bf16_workspace(rows, k) bytes,
  *               8-byte aligned, owned by the caller; its contents on entry do
  *               not matter.  Calls that overlap on the GPU must not share it.
+ *               A call leaves its ticket words cleared, so a call captured in
+ *               a CUDA graph may be replayed on the same workspace.
  *   outputs     as for tf_topk_bf16 with cols = vocab.
  * Asynchronous on `stream`; allocates nothing.  Returns a TF_TOPK_* status:
  * ERR_SHAPE, ERR_K, ERR_NULL, ERR_ALIGN, ERR_SCRATCH (workspace too small),

@@ -112,6 +112,41 @@ def test_two_calls_share_a_workspace():
     assert_same(_np(rb), head_oracle.topk(b.hidden, b.weight, b.k), "second call, same workspace")
 
 
+def test_captured_call_replays():
+    """A call captured in a CUDA graph, replayed on new inputs written into
+    the same buffers (the cut-tile tickets are cleared by each call), matches
+    the oracle every time."""
+    import torch
+
+    from wide_bf16_row_gb300 import topk
+
+    rows, dim, vocab, k = 15, 512, 60000, 16
+    first = synth.head_inputs(rows, dim, vocab, k, seed=21)
+    hid, w = _dev(first.hidden), _dev(first.weight)
+    ws = torch.empty((topk.tf_topk_head_bf16_workspace(rows, k),), dtype=torch.uint8, device="cuda")
+    out = (torch.empty((rows, k), dtype=torch.int32, device="cuda"),
+           torch.empty((rows, k), dtype=torch.int16, device="cuda"),
+           torch.empty((rows,), dtype=torch.int32, device="cuda"),
+           torch.empty((rows,), dtype=torch.int32, device="cuda"))
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        topk.head_topk_bf16(hid, w, k, out=out, workspace=ws, stream=side)  # warm: per-device setup
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        topk.head_topk_bf16(hid, w, k, out=out, workspace=ws, stream=side)
+    for seed in (21, 22, 23, 23):
+        h = synth.head_inputs(rows, dim, vocab, k, seed=seed)
+        hid.copy_(_dev(h.hidden))
+        w.copy_(_dev(h.weight))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert_same(_np(out), head_oracle.topk(h.hidden, h.weight, k), f"replay, seed {seed}")
+    assert topk.device_fault() == 0
+
+
 def test_guards():
     import torch
 

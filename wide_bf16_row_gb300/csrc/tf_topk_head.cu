@@ -888,7 +888,7 @@ template <int P>
 __global__ void __launch_bounds__(kMergeThreads, 1)
 topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *__restrict__ ws_heads, int32_t lists,
                        int32_t k, int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
-                       int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
+                       int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask, uint64_t *__restrict__ tickets)
 {
     constexpr int E = MergeShape<P>::E, G = MergeShape<P>::G;
     extern __shared__ __align__(16) uint64_t merge_dsmem[]; // the row's lists: [lists][P]
@@ -910,6 +910,11 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
         mbar_expect_tx(&bar, bytes);
         bulk_load(merge_dsmem, ws_entries + (size_t)r * lists * P, bytes, &bar);
     }
+    // The head kernel has finished, and with it every use of the split-tile
+    // tickets: clear them, so that the next call on this workspace -- also a
+    // replay of a captured call, which repeats its tag -- starts from empty.
+    if (r == 0)
+        for (int j = tid; j < lists; j += kMergeThreads) tickets[j] = 0;
     uint32_t f = tid < lists ? (uint32_t)(__ldcg(ws_heads + (size_t)r * lists + tid) >> 32) : 0u;
     if (__syncthreads_or(!mbar_wait(&bar, 0))) {
         // the copy did not land in time: report, and wait (bounded) for it
@@ -1013,7 +1018,7 @@ static_assert(kHeadSmemBytes <= 227 * 1024, "the head kernel's shared memory fit
 
 // The merge kernel for each list stride P = 2, 4, .., 64.
 using MergeKernel = void (*)(const uint64_t *, const uint64_t *, int32_t, int32_t, int32_t *, uint16_t *, int32_t *,
-                             uint32_t *);
+                             uint32_t *, uint64_t *);
 constexpr int kMergeKernels = 6;
 const MergeKernel kMergeKernel[kMergeKernels] = {topk_head_merge_kernel<2>,  topk_head_merge_kernel<4>,
                                                  topk_head_merge_kernel<8>,  topk_head_merge_kernel<16>,
@@ -1168,7 +1173,8 @@ int run_head(const void *hidden, const void *weight, int32_t rows, int32_t dim, 
         mcfg.blockDim = dim3(kMergeThreads, 1, 1);
         mcfg.dynamicSmemBytes = kMergeSmemBytes;
         e = cudaLaunchKernelEx(&mcfg, merge_kernel_for(list_stride(k)), (const uint64_t *)ws.lists,
-                               (const uint64_t *)ws.heads, (int32_t)grid, k, out_idx, out_val, out_count, out_mask);
+                               (const uint64_t *)ws.heads, (int32_t)grid, k, out_idx, out_val, out_count, out_mask,
+                               ws.tickets);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return tf_topk_internal_fail_cuda((int)e);
