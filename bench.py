@@ -697,8 +697,10 @@ def run_ours(args) -> None:
 
     per_config = None
     head = None
-    if rank == 0 and world == 1 and not args.no_per_config:
+    tables = "none" if args.no_per_config else args.tables
+    if rank == 0 and world == 1 and tables == "all":
         per_config = per_config_table(dev, peak, not args.no_cpu_baseline, min(0.6, args.cpu_seconds))
+    if rank == 0 and world == 1 and tables in ("all", "head"):
         head = head_table(dev, peak, not args.no_cpu_baseline, min(0.6, args.cpu_seconds))
 
     cpu = None
@@ -777,6 +779,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="issue the timed launches one by one from Python instead of replaying them as a CUDA graph")
+    ap.add_argument("--tables", choices=("all", "head", "none"), default="all",
+                    help="after the timed workload: the per-config and draft-head tables, the head table only, or none")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-workload table (every named workload and sweep points)")
     args = ap.parse_args(argv)
