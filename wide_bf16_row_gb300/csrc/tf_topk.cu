@@ -660,51 +660,15 @@ __device__ __forceinline__ bool spill_hits(uint32_t (&kv)[kVecPerThread][4], uin
     return hit;
 }
 
-// Heavy ties: every key of the chunk that reaches t_floor, in column order, in
-// `stage` (0 elsewhere), re-read from global memory (the registers that held
-// the chunk already carry the next one).  Keys are exact as in fix_keys:
-// columns outside the row and NaN become 0.
-template <int kFmt = kBf16>
-__device__ __noinline__ void restage_chunk(uint4 *stage, const uint4 *vbase, ChunkGeom geo, int32_t cbeg,
-                                           int nvalid, int32_t col_base, uint32_t t_floor)
-{
-    const int tid = threadIdx.x;
-    for (int i = 0; i < kVecPerThread; ++i) {
-        const int lv = i * kThreads + tid;
-        uint32_t qw[4] = {0, 0, 0, 0};
-        if (lv < nvalid) {
-            const int32_t v = cbeg + lv;
-            const uint4 q = (v >= geo.vfull0 && v < geo.vfull1) ? ld_stream(vbase + v)
-                                                               : load_edge_vector(geo.rowp, geo.cols, geo.m, v);
-            const uint32_t raw4[4] = {q.x, q.y, q.z, q.w};
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t key2 = keys_from_raw2(raw4[w]);
-                uint32_t out = 0;
-                for (int h = 0; h < 2; ++h) {
-                    const int32_t c = col_base + lv * 8 + 2 * w + h;
-                    uint32_t key = (key2 >> (16 * h)) & 0xFFFFu;
-                    if (c < 0 || c >= geo.cols || key > Fmt16<kFmt>::kKeyPosInf || key < Fmt16<kFmt>::kKeyNegInf ||
-                        key < t_floor)
-                        key = 0;
-                    out |= key << (16 * h);
-                }
-                qw[w] = out;
-            }
-        }
-        stage[lv] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-    }
-}
-
 // The chunk's candidates (keys >= t_floor) into sm.cand from the spilled
 // slots of the hit threads: each hit thread's warp scans its keys one word
 // per lane.  Returns their number n once every thread has pushed (a barrier);
-// above kCandCap (heavy ties) the chunk is restaged and selected exactly, and
-// n = k.  `base` (block-uniform) is the candidate counter's value before the
+// above kCandCap (heavy ties) the chunk is selected exactly from the spilled
+// keys, and n = k.  `base` (block-uniform) is the candidate counter's value before the
 // chunk and after it.  Block-uniform.
 template <int kFmt = kBf16>
 __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, int k, SmemCore &sm, uint4 *stage,
-                                                    const uint4 *vbase, const ChunkGeom &geo, int32_t cbeg,
-                                                    int nvalid, int32_t col_base, uint32_t &base)
+                                                    uint32_t &base)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __syncwarp();
@@ -718,7 +682,7 @@ __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, 
         uint32_t top = 0;
         if ((key2 & 0xFFFFu) >= t_floor) top = push_candidate(sm, key2 & 0xFFFFu, local, base) + 1u;
         if ((key2 >> 16) >= t_floor) top = push_candidate(sm, key2 >> 16, local + 1, base) + 1u;
-        // past the buffer the chunk is selected exactly from a fresh read:
+        // past the buffer the chunk is selected exactly from the spilled keys:
         // pushing the rest (up to a whole chunk of ties) would only cost atomics
         if (crowded && __any_sync(0xFFFFFFFFu, top > (uint32_t)kCandCap)) break;
     }
@@ -727,7 +691,13 @@ __device__ __forceinline__ uint32_t push_candidates(bool hit, uint32_t t_floor, 
     uint32_t n = total - base;
     base = total;
     if (n > (uint32_t)kCandCap) {
-        restage_chunk<kFmt>(stage, vbase, geo, cbeg, nvalid, col_base, t_floor);
+        // every key that can matter (>= t_floor) was spilled by its thread, in
+        // column order and exact (NaN, out-of-row and past-the-end columns are
+        // key 0); the other threads' slots still hold an earlier chunk
+        if (!hit) {
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) stage[i * kThreads + tid] = make_uint4(0, 0, 0, 0);
+        }
         __syncthreads();
         exact_select<kFmt>(reinterpret_cast<const uint32_t *>(stage), t_floor, k, sm); // counts from 0
         n = sm.n_cand; // == k
@@ -1510,8 +1480,7 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
         const bool more = cend < v_end;
         if (more) load_chunk(kv, vbase, geo, cend, v_end, cols);
         const uint32_t n =
-            push_candidates<kFmt>(hit, t_floor, k, sm, keys, vbase, geo, cbeg, nvalid, col_base, cand_base);
-        if (n > (uint32_t)kCandCap && more) load_chunk(kv, vbase, geo, cend, v_end, cols); // reissued after the exact path
+            push_candidates<kFmt>(hit, t_floor, k, sm, keys, cand_base);
         if (n) merge_candidates(n, col_base, k, sm, run_i, free_i, run_len);
         __syncthreads(); // the merge is complete before the next chunk reads its bound
     }
