@@ -2010,7 +2010,8 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     nnz += nv * (16u / (uint32_t)sizeof(T)) - nan;
     flags = __reduce_or_sync(0xFFFFFFFFu, flags);
     nnz = __reduce_add_sync(0xFFFFFFFFu, nnz);
-    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, t[0]);
+    const uint32_t tmax = t[0]; // this thread's largest key (warp_jth pops the kept lists)
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
     const uint32_t jth = warp_jth<Q>(t, (uint32_t)((k + kWideWarps - 1) / kWideWarps));
     __syncthreads(); // the initialisation above is visible
     if ((tid & 31) == 0) {
@@ -2040,11 +2041,15 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
             if (slot < (uint32_t)kWideCap) sm.ent[slot] = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)c);
         }
     };
-    wide_scan2<T, true>(row, cols, elem2, [&](const uint4 &q, int32_t c0) {
-        uint32_t vmx, vmn;
-        vector_key_range<T>(q, vmx, vmn);
-        if (hi_key<T>(vmx) >= vfloor) vector_elems<T>(q, c0, elem2);
-    });
+    // only a thread whose largest key reaches the bound holds an element that
+    // does: the others skip the second read
+    if (tmax >= bound) {
+        wide_scan2<T, true>(row, cols, elem2, [&](const uint4 &q, int32_t c0) {
+            uint32_t vmx, vmn;
+            vector_key_range<T>(q, vmx, vmn);
+            if (hi_key<T>(vmx) >= vfloor) vector_elems<T>(q, c0, elem2);
+        });
+    }
     __syncthreads();
     const uint32_t n = sm.n_ent;
     const uint64_t *res = sm.ent;
