@@ -1984,22 +1984,40 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
         nnz += key != 0u;
         keep_insert<Q>(t, key);
     };
+    // fp32: once the kept floor is a value >= +0, a vector can reach it only
+    // if its largest raw bits, compared as signed integers, exceed the
+    // floor's (non-negative floats order like their bits; a negative one is a
+    // negative integer): three max operations a vector instead of four keys.
+    // The raw signed and unsigned maxima also show any NaN or infinity.
+    int32_t fr = INT32_MIN, rs = INT32_MIN; // the floor's raw bits (or INT32_MIN: no raw filter yet)
+    uint32_t ru = 0;
     wide_scan2<T, true>(row, cols, elem1, [&](const uint4 &q, int32_t) {
-        uint32_t vmx, vmn;
-        vector_key_range<T>(q, vmx, vmn);
-        if constexpr (sizeof(T) == 2) {
+        if constexpr (sizeof(T) == 4) {
+            const int32_t sv = max(max((int32_t)q.x, (int32_t)q.y), max((int32_t)q.z, (int32_t)q.w));
+            rs = max(rs, sv);
+            ru = max(ru, max(max(q.x, q.y), max(q.z, q.w)));
+            ++nv;
+            if (sv > fr) {
+                vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
+                fr = t[Q - 1] >= 0x80000000u ? (int32_t)(t[Q - 1] ^ 0x80000000u) : INT32_MIN;
+            }
+        } else {
+            uint32_t vmx, vmn;
+            vector_key_range<T>(q, vmx, vmn);
             smx = max_u16x2(smx, vmx);
             smn = min_u16x2(smn, vmn);
-        } else {
-            smx = max(smx, vmx);
-            smn = min(smn, vmn);
+            ++nv;
+            if (hi_key<T>(vmx) > t[Q - 1])
+                vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
         }
-        ++nv;
-        if (hi_key<T>(vmx) > t[Q - 1])
-            vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
     });
+    bool special;
+    if constexpr (sizeof(T) == 4)
+        special = rs >= 0x7F800000 || ru >= 0xFF800000u; // +inf or a positive NaN; -inf or a negative NaN
+    else
+        special = hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey;
     uint32_t nan = 0;
-    if (hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey) {
+    if (special) {
         wide_scan2<T, false>(row, cols, elem1, [&](const uint4 &q, int32_t) {
             vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) {
                 flags |= wide_flag<T, kFmt>(raw);
