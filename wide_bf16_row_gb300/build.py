@@ -9,11 +9,12 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 from pathlib import Path
 
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
-SOURCES = [PKG / "csrc" / "tf_topk.cu", PKG / "csrc" / "tf_topk_head.cu"]
+SOURCES = [PKG / "csrc" / "tf_topk.cu", PKG / "csrc" / "tf_topk_head.cu", PKG / "csrc" / "tf_topk_f32.cu"]
 HEADERS = [ROOT / "include" / "tf_topk.h"]
 LIBRARY = PKG / "libtf_topk.so"
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
@@ -24,9 +25,13 @@ def nvcc() -> str:
     return cand
 
 
-def command(out: Path) -> list[str]:
-    return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
-            "-I", str(ROOT / "include"), "-o", str(out), *map(str, SOURCES)]
+def compile_command(src: Path, obj: Path) -> list[str]:
+    return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-c",
+            "-I", str(ROOT / "include"), "-o", str(obj), str(src)]
+
+
+def link_command(objs: list[Path], out: Path) -> list[str]:
+    return [nvcc(), ARCH, "-shared", "-o", str(out), *map(str, objs)]
 
 
 def up_to_date() -> bool:
@@ -40,11 +45,22 @@ def build(force: bool = False, verbose: bool = False) -> Path:
     if up_to_date() and not force:
         return LIBRARY
     tmp = LIBRARY.with_name(f"{LIBRARY.name}.tmp{os.getpid()}")
-    cmd = command(tmp)
+    objs = [LIBRARY.with_name(f"{src.stem}.tmp{os.getpid()}.o") for src in SOURCES]
+    cmds = [compile_command(src, obj) for src, obj in zip(SOURCES, objs)]
     if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIBRARY)
+        for cmd in cmds:
+            print(" ".join(cmd), file=sys.stderr)
+    try:
+        # the translation units compile side by side, then one link
+        with ThreadPoolExecutor(max_workers=len(cmds)) as pool:
+            for result in pool.map(lambda c: subprocess.run(c, check=True), cmds):
+                pass
+        subprocess.run(link_command(objs, tmp), check=True)
+        os.replace(tmp, LIBRARY)
+    finally:
+        for obj in objs:
+            if obj.exists():
+                obj.unlink()
     return LIBRARY
 
 

@@ -86,6 +86,11 @@ static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocWords];
 
 namespace cg = cooperative_groups;
 
+// fp32 rows with k <= TF_TOPK_MAX_K on the fp32 cluster kernel (tf_topk_f32.cu).
+int tf_topk_internal_select_f32(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int32_t k,
+                                int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_mask,
+                                int sm_count, void *stream);
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -2691,6 +2696,9 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
     const int st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == TF_TOPK_DTYPE_F32 && k <= kMaxK && plan == TF_TOPK_PLAN_AUTO)
+        return tf_topk_internal_select_f32(logits, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
+                                           sm_count, stream);
     if (dtype == TF_TOPK_DTYPE_F16 && k <= kMaxK && plan != TF_TOPK_PLAN_WIDE) {
         // fp16 shares bf16's key map: the cluster plans, with fp16's special values
         int p = plan == TF_TOPK_PLAN_AUTO ? pick_plan(rows, cols, k, sm_count) : plan;
