@@ -184,3 +184,50 @@ def test_f16_bench_shape_auto():
     with np.errstate(over="ignore"):
         x = synth.bf16_to_float(w.logits).astype(np.float16).view(np.uint16)
     assert_same(gpu_select(x, w.cols, w.k, "f16"), oracle.topk(x, w.cols, w.k, dtype="f16"), "f16 256x248320")
+
+
+# fp32 with k <= 64 on AUTO runs the fp32 cluster kernel; the shapes pick its
+# span counts 1, 2, 4 and 8 (one row per SM or more: 2)
+F32_SHAPES = [(6, 5000, 5008), (3, 70001, 70016), (40, 40000, 40000), (160, 20000, 20004)]
+
+
+@pytest.mark.parametrize("rows,cols,stride", F32_SHAPES, ids=lambda v: str(v))
+def test_f32_cluster_kernel(rows, cols, stride):
+    """fp32, k <= 64, AUTO (the fp32 cluster kernel): mixed rows with every
+    fp32 special, copies and low-half near-ties, padded strides, row bases
+    off the 16-byte grid, against the oracle."""
+    x = gen("f32", rows, cols, 11 + rows, stride, special_frac=0.02, dup_frac=0.05)
+    for k in (1, 20, 33, 64):
+        assert_same(gpu_select(x, cols, k, "f32"), oracle.topk(x, cols, k, dtype="f32"), f"f32 {rows}x{cols} k{k}")
+    for offset in (1, 2, 3):
+        assert_same(gpu_select(x, cols, 20, "f32", offset=offset), oracle.topk(x, cols, 20, dtype="f32"),
+                    f"f32 {rows}x{cols} offset {offset}")
+
+
+@pytest.mark.parametrize("cols", [5000, 70001])
+def test_f32_cluster_kernel_ties_and_specials(cols):
+    """Heavy ties (the exact path) and special rows on the fp32 cluster kernel."""
+    rng = np.random.default_rng(cols)
+    ties = np.zeros((6, cols), np.uint32)
+    ties[0] = rng.integers(0, 2, size=cols).astype(np.uint32) << np.uint32(31)         # +-0
+    ties[1] = rng.choice(np.array([0x3F800000, 0x40000000, 0xBF800000], np.uint32), size=cols)
+    ties[2] = 0x7FC00000                                                               # all NaN
+    ties[3] = rng.choice(np.array([0x7F800000, 0xFF800000, 0x00000001, 0x80000001, 0xFFFFFFFF], np.uint32),
+                         size=cols)                                                    # infs, subnormals, a NaN
+    ties[4] = (rng.standard_normal(cols) * 2).astype(np.float32).view(np.uint32)
+    ties[5] = np.float32(-3.5).view(np.uint32)                                         # one negative value
+    for k in (1, 20, 64):
+        assert_same(gpu_select(ties, cols, k, "f32"), oracle.topk(ties, cols, k, dtype="f32"), f"f32 ties k{k}")
+
+
+def test_f32_cluster_kernel_short_rows_and_bench_shape():
+    """Rows shorter than k, and the bench workload's values widened to fp32
+    (256 x 248320, AUTO) against the oracle and against the wide kernel."""
+    x = gen("f32", 4, 37, 5, 40)
+    assert_same(gpu_select(x, 37, 64, "f32"), oracle.topk(x, 37, 64, dtype="f32"), "f32 37 columns k64")
+    w = synth.config_draft_window()
+    x = (np.asarray(w.logits, np.uint32) << np.uint32(16)).astype(np.uint32)
+    exp = oracle.topk(x[:32], w.cols, w.k, dtype="f32")
+    got = gpu_select(x, w.cols, w.k, "f32")
+    assert_same(tuple(a[:32] for a in got), exp, "f32 256x248320 (first 32 rows)")
+    assert_same(got, gpu_select(x, w.cols, w.k, "f32", plan=64), "f32 256x248320 cluster vs wide")
