@@ -276,10 +276,13 @@ int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows
  * bf16 with k <= TF_TOPK_MAX_K runs the plans of tf_topk_bf16 (the same
  * results, byte for byte).  fp16 with k <= TF_TOPK_MAX_K runs the cluster
  * plans (it shares bf16's order-preserving key map; only its special values
- * differ), except where AUTO would give a row one CTA.  Everything else runs
- * the wide kernel: one CTA per row, two passes over the row (a bound from
- * each thread's best keys, then every element reaching it, ranked), with an
- * exact counting search when ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
+ * differ), except where AUTO would give a row one CTA.  fp32 with k <=
+ * TF_TOPK_MAX_K on AUTO runs the fp32 cluster kernel: each row's column spans
+ * over a thread-block cluster, read once against a running bound, on 32-bit
+ * keys.  Everything else (and TF_TOPK_PLAN_WIDE) runs the wide kernel: one
+ * CTA per row, two passes over the row (a bound from each thread's best keys,
+ * then every element reaching it, ranked), with an exact counting search when
+ * ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
  * Returns a TF_TOPK_* status: ERR_DTYPE for an unknown format, ERR_K,
  * ERR_SHAPE, ERR_NULL, ERR_ALIGN as for tf_topk_bf16.
  */
