@@ -1706,8 +1706,8 @@ topk_nucleus_kernel(const T *__restrict__ val, const int32_t *__restrict__ count
 // The same order (score descending, lower column first; NaN never selected,
 // +0 == -0) for bf16, fp16 and fp32 rows and k up to TF_TOPK_MAX_K_WIDE.  One
 // CTA per row, in two passes over the row:
-//   1. each thread keeps the keys of its Q best elements (distinct elements;
-//      Q = 4, or 16 for k > 256), and the CTA takes the row's non-finite mask
+//   1. each thread keeps the keys of its Q = 4 best elements (distinct
+//      elements), and the CTA takes the row's non-finite mask
 //      and its count of numbers.  Each warp finds the j-th largest of its
 //      lanes' kept keys, j = ceil(k / warps), so B = the smallest of those is
 //      reached by at least k elements of the row;
@@ -1726,8 +1726,11 @@ constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideUnroll = 8;                  // 16-byte loads in flight per thread
 constexpr int kWideCap = 4096;                  // entries pass 2 may collect
 constexpr int kWideMaxK = TF_TOPK_MAX_K_WIDE;
-constexpr int kWideSmallK = 256;                // k up to this keeps 4 keys a thread, above it 16
-static_assert(32 * 4 >= (kWideSmallK + kWideWarps - 1) / kWideWarps, "a warp keeps j keys (small k)");
+constexpr int kWideKeep = 4;                    // keys a thread keeps in the first pass
+// a warp's 32 lanes keep at least the j = ceil(k / warps) keys its bound
+// counts, for every k (more kept keys made the bound tighter but the first
+// pass slower: 16 for k = 1024 cost 239k cycles a row against about 100k)
+static_assert(32 * kWideKeep >= (TF_TOPK_MAX_K_WIDE + kWideWarps - 1) / kWideWarps, "a warp keeps j keys");
 static_assert(32 * 16 >= (kWideMaxK + kWideWarps - 1) / kWideWarps, "a warp keeps j keys (large k)");
 static_assert(kWideCap >= kWideMaxK, "a short row's numbers all fit");
 
@@ -2730,23 +2733,16 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
             return TF_TOPK_OK;
         }
     }
-    const bool small = k <= kWideSmallK;
     switch (dtype) {
     case TF_TOPK_DTYPE_BF16:
-        return small ? launch_wide<uint16_t, TF_TOPK_DTYPE_BF16, 4>(logits, rows, cols, row_stride, k, out_idx,
-                                                                    out_val, out_count, out_mask, s)
-                     : launch_wide<uint16_t, TF_TOPK_DTYPE_BF16, 16>(logits, rows, cols, row_stride, k, out_idx,
-                                                                     out_val, out_count, out_mask, s);
+        return launch_wide<uint16_t, TF_TOPK_DTYPE_BF16, kWideKeep>(logits, rows, cols, row_stride, k, out_idx,
+                                                                    out_val, out_count, out_mask, s);
     case TF_TOPK_DTYPE_F16:
-        return small ? launch_wide<uint16_t, TF_TOPK_DTYPE_F16, 4>(logits, rows, cols, row_stride, k, out_idx,
-                                                                   out_val, out_count, out_mask, s)
-                     : launch_wide<uint16_t, TF_TOPK_DTYPE_F16, 16>(logits, rows, cols, row_stride, k, out_idx,
-                                                                    out_val, out_count, out_mask, s);
+        return launch_wide<uint16_t, TF_TOPK_DTYPE_F16, kWideKeep>(logits, rows, cols, row_stride, k, out_idx,
+                                                                   out_val, out_count, out_mask, s);
     default:
-        return small ? launch_wide<uint32_t, TF_TOPK_DTYPE_F32, 4>(logits, rows, cols, row_stride, k, out_idx,
-                                                                   out_val, out_count, out_mask, s)
-                     : launch_wide<uint32_t, TF_TOPK_DTYPE_F32, 16>(logits, rows, cols, row_stride, k, out_idx,
-                                                                    out_val, out_count, out_mask, s);
+        return launch_wide<uint32_t, TF_TOPK_DTYPE_F32, kWideKeep>(logits, rows, cols, row_stride, k, out_idx,
+                                                                   out_val, out_count, out_mask, s);
     }
 }
 
