@@ -1733,6 +1733,13 @@ constexpr int kWideKeep = 4;                    // keys a thread keeps in the fi
 static_assert(32 * kWideKeep >= (TF_TOPK_MAX_K_WIDE + kWideWarps - 1) / kWideWarps, "a warp keeps j keys");
 static_assert(32 * 16 >= (kWideMaxK + kWideWarps - 1) / kWideWarps, "a warp keeps j keys (large k)");
 static_assert(kWideCap >= kWideMaxK, "a short row's numbers all fit");
+// The first pass writes each 8 elements' largest key (its upper 16 bits) to a
+// table in shared memory, so the second reads back only the vectors whose
+// largest key reaches the bound; rows too wide for the table (or whose table
+// has more than kWideList such entries) read the whole row again.
+constexpr int kWideTbl = 32768;                 // entries: rows up to 262144 columns
+constexpr int kWideList = 2048;                 // table entries the second pass may take
+static_assert(kWideTbl % (8 * kWideThreads) == 0 && kWideList % kWideThreads == 0, "whole rounds");
 
 // Order-preserving key of one element (0 for NaN, +0 and -0 one key), and
 // its non-finite flag (1 NaN, 2 +inf, 4 -inf).
@@ -1795,6 +1802,15 @@ __device__ __forceinline__ uint32_t wide_flag(uint32_t raw)
     return 0u;
 }
 
+// Elements before the row's first 16-byte boundary (all of a short row).
+template <typename T>
+__device__ __forceinline__ int32_t wide_head(const T *row, int32_t cols)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    const int32_t head = (int32_t)(((16u - (uint32_t)(a & 15u)) & 15u) / sizeof(T));
+    return head < cols ? head : cols;
+}
+
 // Every column of the row, each thread a strided share: the row's unaligned
 // head and tail through f(column, raw bits), the 16-byte-aligned body
 // through g(vector, its first column), kWideUnroll vectors a thread in flight
@@ -1804,13 +1820,12 @@ __device__ __forceinline__ void wide_scan2(const T *row, int32_t cols, Fe &&f, F
 {
     constexpr int kPer = 16 / (int)sizeof(T);
     const int tid = threadIdx.x;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(row);
-    int32_t head = (int32_t)(((16u - (uint32_t)(a & 15u)) & 15u) / sizeof(T));
-    if (head > cols) head = cols;
+    const int32_t head = wide_head(row, cols);
     if constexpr (kEdges)
         for (int32_t c = tid; c < head; c += kWideThreads) f(c, (uint32_t)row[c]);
     const int32_t nvec = (cols - head) / kPer;
     const uint4 *v = reinterpret_cast<const uint4 *>(row + head);
+    // the last batch too is issued whole (its loads guarded), not one by one
     int32_t i = tid;
     for (; i + (kWideUnroll - 1) * kWideThreads < nvec; i += kWideUnroll * kWideThreads) {
         uint4 q[kWideUnroll];
@@ -1914,9 +1929,11 @@ __device__ __forceinline__ uint32_t wide_block_sum(uint32_t v, uint32_t *red)
 struct __align__(16) WideSmem {
     uint64_t ent[kWideCap];
     uint64_t sorted[kWideThreads];           // ranked entries when few
+    uint16_t tbl[kWideTbl];                  // the upper 16 bits of each 8 elements' largest key
+    uint32_t list[kWideList];                // table entries that reach the bound
     uint32_t red[kWideWarps];
     uint32_t warp_b[kWideWarps];
-    uint32_t n_ent, flags, nnz, kmax;
+    uint32_t n_ent, flags, nnz, kmax, n_list;
 };
 
 // Keep the Q largest keys seen (t[0] >= ... >= t[Q-1]; 0 = empty).
@@ -1974,56 +1991,89 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
         sm.flags = 0;
         sm.nnz = 0;
         sm.kmax = 0;
+        sm.n_list = 0;
     }
 
-    // ---- pass 1: each thread's Q best keys, the mask, the count of numbers.
-    // A vector's elements are looked at one by one only when its max raw key
-    // passes the thread's kept floor; the mask and the NaN count come from a
-    // second look at the thread's vectors, taken only when its raw keys reached
-    // an infinity's.
+    // ---- pass 1: each thread's Q largest vector maxima (a vector's largest
+    // key: distinct vectors, distinct elements, so a warp's j-th largest kept
+    // maximum still has j elements at or above it), the mask, the count of
+    // numbers, and the table of maxima.
     using FK = WideKeys<T, kFmt>;
+    constexpr int kPer = 16 / (int)sizeof(T);
+    constexpr int G = 8 / kPer; // vectors a table entry covers (the thread's consecutive ones)
     uint32_t t[Q];
 #pragma unroll
     for (int i = 0; i < Q; ++i) t[i] = 0;
-    uint32_t flags = 0, nnz = 0, smx = 0, smn = 0xFFFFFFFFu, nv = 0;
+    uint32_t flags = 0, nnz = 0, smx = 0, smn = 0xFFFFFFFFu;
     auto elem1 = [&](int32_t, uint32_t raw) {
         const uint32_t key = wide_key<T, kFmt>(raw);
         flags |= wide_flag<T, kFmt>(raw);
         nnz += key != 0u;
         keep_insert<Q>(t, key);
     };
-    // fp32: once the kept floor is a value >= +0, a vector can reach it only
-    // if its largest raw bits, compared as signed integers, exceed the
-    // floor's (non-negative floats order like their bits; a negative one is a
-    // negative integer): three max operations a vector instead of four keys.
-    // The raw signed and unsigned maxima also show any NaN or infinity.
-    int32_t fr = INT32_MIN, rs = INT32_MIN; // the floor's raw bits (or INT32_MIN: no raw filter yet)
-    uint32_t ru = 0;
-    wide_scan2<T, true>(row, cols, elem1, [&](const uint4 &q, int32_t) {
-        if constexpr (sizeof(T) == 4) {
-            const int32_t sv = max(max((int32_t)q.x, (int32_t)q.y), max((int32_t)q.z, (int32_t)q.w));
-            rs = max(rs, sv);
-            ru = max(ru, max(max(q.x, q.y), max(q.z, q.w)));
-            ++nv;
-            if (sv > fr) {
-                vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
-                fr = t[Q - 1] >= 0x80000000u ? (int32_t)(t[Q - 1] ^ 0x80000000u) : INT32_MIN;
-            }
-        } else {
-            uint32_t vmx, vmn;
-            vector_key_range<T>(q, vmx, vmn);
+    // a vector's largest key: its largest raw key, unless that is a NaN's
+    // (a positive NaN: the elements are looked at one by one; only negative
+    // NaNs: no number) or -0's
+    auto vec1 = [&](const uint4 &q) -> uint32_t {
+        uint32_t vmx, vmn;
+        vector_key_range<T>(q, vmx, vmn);
+        if constexpr (sizeof(T) == 2) {
             smx = max_u16x2(smx, vmx);
             smn = min_u16x2(smn, vmn);
-            ++nv;
-            if (hi_key<T>(vmx) > t[Q - 1])
-                vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { keep_insert<Q>(t, wide_key<T, kFmt>(raw)); });
+        } else {
+            smx = max(smx, vmx);
+            smn = min(smn, vmn);
         }
-    });
-    bool special;
-    if constexpr (sizeof(T) == 4)
-        special = rs >= 0x7F800000 || ru >= 0xFF800000u; // +inf or a positive NaN; -inf or a negative NaN
-    else
-        special = hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey;
+        uint32_t vk = hi_key<T>(vmx);
+        if (vk > FK::kPosInfKey) {
+            vk = 0;
+            vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) { vk = max(vk, wide_key<T, kFmt>(raw)); });
+        } else if (vk < FK::kNegInfKey) {
+            vk = 0;
+        } else if (vk == F::kSign - 1u) {
+            vk = F::kSign; // -0: +0's key
+        }
+        keep_insert<Q>(t, vk);
+        return vk;
+    };
+    const int32_t head = wide_head(row, cols);
+    for (int32_t c = tid; c < head; c += kWideThreads) elem1(c, (uint32_t)row[c]);
+    const int32_t nvec = (cols - head) / kPer;
+    const uint4 *v = reinterpret_cast<const uint4 *>(row + head);
+    // this thread's vectors: tid + s * threads for positions s < P; table
+    // entry tid + w * threads covers positions G w .. G w + G - 1
+    const int32_t P = tid < nvec ? (nvec - 1 - tid) / kWideThreads + 1 : 0;
+    const int32_t W0 = ((nvec + kWideThreads - 1) / kWideThreads + G - 1) / G;
+    const int32_t nent = W0 * kWideThreads;
+    const bool use_tbl = nent <= kWideTbl;
+    uint32_t pend = 0; // G = 2: the first vector's maximum of an entry
+    for (int32_t i = tid, s0 = 0; i < nvec; i += kWideUnroll * kWideThreads, s0 += kWideUnroll) {
+        uint4 q[kWideUnroll];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u)
+            if (i + u * kWideThreads < nvec) q[u] = v[i + u * kWideThreads];
+#pragma unroll
+        for (int u = 0; u < kWideUnroll; ++u) {
+            if (i + u * kWideThreads < nvec) {
+                const uint32_t vk = vec1(q[u]);
+                if constexpr (G == 1) {
+                    if (use_tbl) sm.tbl[i + u * kWideThreads] = (uint16_t)vk;
+                } else if (u & 1) {
+                    if (use_tbl) sm.tbl[tid + ((s0 + u) >> 1) * kWideThreads] = (uint16_t)(max(pend, vk) >> 16);
+                } else {
+                    pend = vk;
+                }
+            }
+        }
+    }
+    if (use_tbl) {
+        if constexpr (G == 2)
+            if (P & 1) sm.tbl[tid + (P >> 1) * kWideThreads] = (uint16_t)(pend >> 16);
+        for (int32_t w = (P + G - 1) / G; w < W0; ++w) sm.tbl[tid + w * kWideThreads] = 0;
+    }
+    for (int32_t c = head + nvec * kPer + tid; c < cols; c += kWideThreads) elem1(c, (uint32_t)row[c]);
+    const uint32_t nv = (uint32_t)P;
+    const bool special = hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey;
     uint32_t nan = 0;
     if (special) {
         wide_scan2<T, false>(row, cols, elem1, [&](const uint4 &q, int32_t) {
@@ -2067,9 +2117,63 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
             if (slot < (uint32_t)kWideCap) sm.ent[slot] = ((uint64_t)key << 32) | (uint64_t)(~(uint32_t)c);
         }
     };
-    // only a thread whose largest key reaches the bound holds an element that
-    // does: the others skip the second read
-    if (tmax >= bound) {
+    bool full = !use_tbl;
+    if (use_tbl) {
+        // the table's entries that reach the bound, listed
+        const uint32_t vf16 = sizeof(T) == 2 ? vfloor : vfloor >> 16;
+        const uint32_t vf2 = vf16 | (vf16 << 16);
+        const uint4 *tb = reinterpret_cast<const uint4 *>(sm.tbl);
+        for (int32_t m = tid; m < nent / 8; m += kWideThreads) {
+            const uint4 c = tb[m];
+            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t ge = __vcmpgeu2(w[j], vf2);
+                if (ge & 0xFFFFu) {
+                    const uint32_t slot = atomicAdd(&sm.n_list, 1u);
+                    if (slot < (uint32_t)kWideList) sm.list[slot] = (uint32_t)(8 * m + 2 * j);
+                }
+                if (ge >> 16) {
+                    const uint32_t slot = atomicAdd(&sm.n_list, 1u);
+                    if (slot < (uint32_t)kWideList) sm.list[slot] = (uint32_t)(8 * m + 2 * j + 1);
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t nl = sm.n_list;
+        full = nl > (uint32_t)kWideList;
+        if (!full) {
+            // their vectors, four loads of a thread issued before any is used
+            constexpr int X = 4 / G;
+            for (int32_t j0 = tid; j0 < (int32_t)nl; j0 += X * kWideThreads) {
+                uint4 q[X * G];
+                int32_t vi[X * G];
+#pragma unroll
+                for (int x = 0; x < X; ++x) {
+                    const int32_t j = j0 + x * kWideThreads;
+                    const uint32_t e = j < (int32_t)nl ? sm.list[j] : 0xFFFFFFFFu;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        int32_t idx = -1;
+                        if (e != 0xFFFFFFFFu) {
+                            idx = (int32_t)(e % kWideThreads) + ((int32_t)(e / kWideThreads) * G + g) * kWideThreads;
+                            if (idx >= nvec) idx = -1;
+                        }
+                        vi[x * G + g] = idx;
+                        if (idx >= 0) q[x * G + g] = v[idx];
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < X * G; ++x)
+                    if (vi[x] >= 0) vector_elems<T>(q[x], head + vi[x] * kPer, elem2);
+            }
+            for (int32_t c = tid; c < head; c += kWideThreads) elem2(c, (uint32_t)row[c]);
+            for (int32_t c = head + nvec * kPer + tid; c < cols; c += kWideThreads) elem2(c, (uint32_t)row[c]);
+        }
+    }
+    // otherwise the whole row again: only a thread whose largest key reaches
+    // the bound holds an element that does; the others skip the second read
+    if (full && tmax >= bound) {
         wide_scan2<T, true>(row, cols, elem2, [&](const uint4 &q, int32_t c0) {
             uint32_t vmx, vmn;
             vector_key_range<T>(q, vmx, vmn);
