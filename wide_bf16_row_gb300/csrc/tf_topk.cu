@@ -1740,6 +1740,7 @@ static_assert(kWideCap >= kWideMaxK, "a short row's numbers all fit");
 constexpr int kWideTbl = 32768;                 // entries: rows up to 262144 columns
 constexpr int kWideList = 2048;                 // table entries the second pass may take
 static_assert(kWideTbl % (8 * kWideThreads) == 0 && kWideList % kWideThreads == 0, "whole rounds");
+static_assert(kWideTbl * 2 >= kWideCap * 8 && kWideCap == 4096 && kWideThreads == 512, "the sort's buffers");
 
 // Order-preserving key of one element (0 for NaN, +0 and -0 one key), and
 // its non-finite flag (1 NaN, 2 +inf, 4 -inf).
@@ -1930,6 +1931,7 @@ struct __align__(16) WideSmem {
     uint64_t ent[kWideCap];
     uint64_t sorted[kWideThreads];           // ranked entries when few
     uint16_t tbl[kWideTbl];                  // the upper 16 bits of each 8 elements' largest key
+                                             // (then the sort's second buffer)
     uint32_t list[kWideList];                // table entries that reach the bound
     uint32_t red[kWideWarps];
     uint32_t warp_b[kWideWarps];
@@ -1951,24 +1953,112 @@ __device__ __forceinline__ void keep_insert(uint32_t (&t)[Q], uint32_t key)
     }
 }
 
-// The j-th largest of the warp's kept keys (lanes' lists sorted, popped from
-// the head), or 0 when the warp holds fewer than j nonzero keys.  Warp-uniform.
-template <int Q>
-__device__ __forceinline__ uint32_t warp_jth(uint32_t (&t)[Q], uint32_t j)
+// The j-th largest of the warp's kept keys (counted with repeats), or 0 when
+// the warp holds fewer than j nonzero keys: the largest x with at least j
+// keys >= x, built bit by bit from the top of a kBits-bit key.  Warp-uniform.
+template <int Q, int kBits>
+__device__ __forceinline__ uint32_t warp_jth(const uint32_t (&t)[Q], uint32_t j)
 {
-    uint32_t cnt = 0;
-    for (uint32_t it = 0; it < j; ++it) {
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, t[0]);
-        if (m == 0) return 0;
-        cnt += __popc(__ballot_sync(0xFFFFFFFFu, t[0] == m));
-        if (cnt >= j) return m;
-        if (t[0] == m) {
+    uint32_t x = 0;
+#pragma unroll 1
+    for (int b = kBits - 1; b >= 0; --b) {
+        const uint32_t c = x | (1u << b);
+        uint32_t n = 0;
 #pragma unroll
-            for (int i = 0; i < Q - 1; ++i) t[i] = t[i + 1];
-            t[Q - 1] = 0;
+        for (int i = 0; i < Q; ++i) n += t[i] >= c;
+        if (__reduce_add_sync(0xFFFFFFFFu, n) >= j) x = c;
+    }
+    return x;
+}
+
+// Slots for c items of every lane of the warp (all 32 lanes call): the
+// lane's first slot, one atomic on the counter for the whole warp.
+__device__ __forceinline__ uint32_t warp_reserve(uint32_t c, uint32_t *counter)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += u;
+    }
+    uint32_t base = 0;
+    if (lane == 31 && incl != 0) base = atomicAdd(counter, incl);
+    return __shfl_sync(0xFFFFFFFFu, base, 31) + incl - c;
+}
+
+// Descending sort of s[0..16 * 32 R) into s or u (the one returned), every
+// thread of the CTA taking part.  Each warp sorts a run of 32 R entries in
+// registers (a bitonic network: element r * 32 + lane in e[r], partners a
+// lane apart exchanged by shuffles, the others within the thread), then four
+// rounds merge pairs of runs through shared memory, each thread placing R
+// consecutive outputs found by a merge-path search (the final round only
+// those below `need`).  Entries equal only when they are padding.
+template <int R>
+__device__ uint64_t *wide_sort(uint64_t *s, uint64_t *u, int need)
+{
+    constexpr int L0 = 32 * R, N = 16 * L0;
+    static_assert(kWideWarps == 16, "16 runs");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t e[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) e[r] = s[warp * L0 + r * 32 + lane];
+#pragma unroll
+    for (int size = 2; size <= L0; size <<= 1) {
+#pragma unroll
+        for (int d = size >> 1; d > 0; d >>= 1) {
+            if (d >= 32) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int pr = r ^ (d >> 5);
+                    if (pr > r) {
+                        const bool desc = ((r * 32 + lane) & size) == 0;
+                        const uint64_t hi = max(e[r], e[pr]), lo = min(e[r], e[pr]);
+                        e[r] = desc ? hi : lo;
+                        e[pr] = desc ? lo : hi;
+                    }
+                }
+            } else {
+                const bool lower = (lane & d) == 0;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const bool desc = ((r * 32 + lane) & size) == 0;
+                    const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, e[r], d);
+                    e[r] = (lower == desc) ? max(e[r], o) : min(e[r], o);
+                }
+            }
         }
     }
-    return 0; // not reached: every step pops at least one key
+#pragma unroll
+    for (int r = 0; r < R; ++r) s[warp * L0 + r * 32 + lane] = e[r];
+    __syncthreads();
+    uint64_t *src = s, *dst = u;
+#pragma unroll 1
+    for (int L = L0; L < N; L <<= 1) {
+        const int o0 = threadIdx.x * R;
+        if (2 * L < N || o0 < need) {
+            const int base = o0 & ~(2 * L - 1), d = o0 - base;
+            const uint64_t *A = src + base, *B = A + L;
+            // a: how many of the first d outputs come from A (A first only when larger)
+            int lo = max(0, d - L), hi = min(d, L);
+            while (lo < hi) {
+                const int m = (lo + hi) >> 1;
+                if (A[m] > B[d - 1 - m]) lo = m + 1;
+                else hi = m;
+            }
+            int a = lo, b = d - lo;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const bool takeA = b >= L || (a < L && A[a] > B[b]);
+                dst[o0 + r] = takeA ? A[a++] : B[b++];
+            }
+        }
+        __syncthreads();
+        uint64_t *x = src;
+        src = dst;
+        dst = x;
+    }
+    return src;
 }
 
 template <typename T, int kFmt, int Q>
@@ -2086,9 +2176,9 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     nnz += nv * (16u / (uint32_t)sizeof(T)) - nan;
     flags = __reduce_or_sync(0xFFFFFFFFu, flags);
     nnz = __reduce_add_sync(0xFFFFFFFFu, nnz);
-    const uint32_t tmax = t[0]; // this thread's largest key (warp_jth pops the kept lists)
+    const uint32_t tmax = t[0]; // this thread's largest key
     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, tmax);
-    const uint32_t jth = warp_jth<Q>(t, (uint32_t)((k + kWideWarps - 1) / kWideWarps));
+    const uint32_t jth = warp_jth<Q, 8 * (int)sizeof(T)>(t, (uint32_t)((k + kWideWarps - 1) / kWideWarps));
     __syncthreads(); // the initialisation above is visible
     if ((tid & 31) == 0) {
         atomicOr(&sm.flags, flags);
@@ -2119,38 +2209,37 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     };
     bool full = !use_tbl;
     if (use_tbl) {
-        // the table's entries that reach the bound, listed
+        // the table's entries that reach the bound, listed (nent / 8 is a
+        // multiple of 32: every warp takes whole rounds)
         const uint32_t vf16 = sizeof(T) == 2 ? vfloor : vfloor >> 16;
         const uint32_t vf2 = vf16 | (vf16 << 16);
         const uint4 *tb = reinterpret_cast<const uint4 *>(sm.tbl);
         for (int32_t m = tid; m < nent / 8; m += kWideThreads) {
             const uint4 c = tb[m];
-            const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+            const uint32_t ge[4] = {__vcmpgeu2(c.x, vf2), __vcmpgeu2(c.y, vf2), __vcmpgeu2(c.z, vf2),
+                                    __vcmpgeu2(c.w, vf2)};
+            uint32_t hits = 0; // bit i: entry 8 m + i
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t ge = __vcmpgeu2(w[j], vf2);
-                if (ge & 0xFFFFu) {
-                    const uint32_t slot = atomicAdd(&sm.n_list, 1u);
-                    if (slot < (uint32_t)kWideList) sm.list[slot] = (uint32_t)(8 * m + 2 * j);
-                }
-                if (ge >> 16) {
-                    const uint32_t slot = atomicAdd(&sm.n_list, 1u);
-                    if (slot < (uint32_t)kWideList) sm.list[slot] = (uint32_t)(8 * m + 2 * j + 1);
-                }
+            for (int j = 0; j < 4; ++j) hits |= ((ge[j] & 1u) | ((ge[j] >> 15) & 2u)) << (2 * j);
+            if (__any_sync(0xFFFFFFFFu, hits != 0)) {
+                uint32_t slot = warp_reserve(__popc(hits), &sm.n_list);
+                for (uint32_t h = hits; h != 0; h &= h - 1, ++slot)
+                    if (slot < (uint32_t)kWideList) sm.list[slot] = (uint32_t)(8 * m + __ffs(h) - 1);
             }
         }
         __syncthreads();
         const uint32_t nl = sm.n_list;
         full = nl > (uint32_t)kWideList;
         if (!full) {
-            // their vectors, four loads of a thread issued before any is used
+            // their vectors, four loads of a thread issued before any is used;
+            // a warp reserves the slots of its entries at once
             constexpr int X = 4 / G;
-            for (int32_t j0 = tid; j0 < (int32_t)nl; j0 += X * kWideThreads) {
+            for (int32_t j0 = 0; j0 < (int32_t)nl; j0 += X * kWideThreads) {
                 uint4 q[X * G];
                 int32_t vi[X * G];
 #pragma unroll
                 for (int x = 0; x < X; ++x) {
-                    const int32_t j = j0 + x * kWideThreads;
+                    const int32_t j = j0 + tid + x * kWideThreads;
                     const uint32_t e = j < (int32_t)nl ? sm.list[j] : 0xFFFFFFFFu;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
@@ -2164,8 +2253,32 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
                     }
                 }
 #pragma unroll
-                for (int x = 0; x < X * G; ++x)
-                    if (vi[x] >= 0) vector_elems<T>(q[x], head + vi[x] * kPer, elem2);
+                for (int x = 0; x < X * G; ++x) {
+                    uint32_t keys[kPer];
+                    uint32_t c = 0;
+                    if (vi[x] >= 0) {
+                        int32_t at = 0;
+                        vector_elems<T>(q[x], 0, [&](int32_t, uint32_t raw) {
+                            keys[at] = wide_key<T, kFmt>(raw);
+                            c += keys[at] >= bound;
+                            ++at;
+                        });
+                    }
+                    if (__any_sync(0xFFFFFFFFu, c != 0)) {
+                        uint32_t slot = warp_reserve(c, &sm.n_ent);
+                        if (c != 0) {
+                            const int32_t c0 = head + vi[x] * kPer;
+#pragma unroll
+                            for (int i = 0; i < kPer; ++i) {
+                                if (keys[i] >= bound) {
+                                    if (slot < (uint32_t)kWideCap)
+                                        sm.ent[slot] = ((uint64_t)keys[i] << 32) | (uint64_t)(~(uint32_t)(c0 + i));
+                                    ++slot;
+                                }
+                            }
+                        }
+                    }
+                }
             }
             for (int32_t c = tid; c < head; c += kWideThreads) elem2(c, (uint32_t)row[c]);
             for (int32_t c = head + nvec * kPer + tid; c < cols; c += kWideThreads) elem2(c, (uint32_t)row[c]);
@@ -2194,11 +2307,15 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
         __syncthreads();
         res = sm.sorted;
     } else if (n <= (uint32_t)kWideCap) {
-        int pn = 1;
+        int pn = 1024;
         while (pn < (int)n) pn <<= 1;
         for (int i = (int)n + tid; i < pn; i += kWideThreads) sm.ent[i] = 0; // pads sort last
         __syncthreads();
-        bitonic_desc(sm.ent, pn);
+        // the table is free now: the merges' second buffer
+        uint64_t *u = reinterpret_cast<uint64_t *>(sm.tbl);
+        if (pn == 1024) res = wide_sort<2>(sm.ent, u, k);
+        else if (pn == 2048) res = wide_sort<4>(sm.ent, u, k);
+        else res = wide_sort<8>(sm.ent, u, k);
     } else {
         __syncthreads(); // every thread has read n before n_ent is reused below
         // ---- heavy ties: K* by a 16-ary search on counts, kmax + 1 counts 0
