@@ -905,6 +905,9 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
     }
     __syncthreads();
     grid_dependency_wait();
+    // the next call's head kernel may be scheduled now: its CTAs set up on the
+    // SMs the head kernel left, and wait for this grid before touching memory
+    grid_dependents_go();
     if (tid == 0) {
         const uint32_t bytes = (uint32_t)lists * P * (uint32_t)sizeof(uint64_t);
         mbar_expect_tx(&bar, bytes);
