@@ -824,6 +824,7 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
 
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kLeadCap = 512; // entries at or above the k-th lead the merge ranks directly
 // The row's lists in shared memory; more than half of an SM's, so that merge
 // CTAs scheduled early (while the head kernel still runs) take an SM each.
 constexpr uint32_t kMergeSmemBytes = 120 * 1024;
@@ -893,6 +894,10 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
     constexpr int E = MergeShape<P>::E, G = MergeShape<P>::G;
     extern __shared__ __align__(16) uint64_t merge_dsmem[]; // the row's lists: [lists][P]
     __shared__ uint64_t part[2][kMergeWarps][P];
+    __shared__ uint64_t lead[kMaxGrid];             // each list's first entry
+    __shared__ uint64_t cand[kLeadCap];             // the entries at or above the k-th lead
+    __shared__ uint64_t kth_lead;
+    __shared__ uint32_t wsum[kMergeWarps];
     __shared__ uint64_t bar;
     __shared__ uint32_t flags;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -926,8 +931,69 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
         mbar_wait(&bar, 0);
         return;
     }
-    // per lane group two running lists (two independent chains), starting
-    // empty; list j enters as max with its reverse, then a sort
+    f = __reduce_or_sync(0xFFFFFFFFu, f);
+    if (lane == 0 && f) atomicOr(&flags, f);
+
+    // The usual case: b, the k-th largest of the lists' first entries, has k
+    // entries at or above it, so only entries >= b can be in the row's top k.
+    // They are few (about k): each list gives its leading ones, and each
+    // takes its place by rank among them.
+    const uint64_t m = tid < lists ? merge_dsmem[(size_t)tid * P] : 0ull;
+    if (tid < lists) lead[tid] = m;
+    if (tid == 0) kth_lead = 0;
+    __syncthreads();
+    if (m != 0) {
+        uint32_t above = 0;
+        for (int u = 0; u < lists; ++u) above += lead[u] > m;
+        if (above == (uint32_t)(k - 1)) kth_lead = m; // leads are distinct: one thread
+    }
+    __syncthreads();
+    const uint64_t bnd = kth_lead;
+    if (bnd != 0) { // else fewer than k lists hold an entry
+        uint32_t c = 0;
+        if (tid < lists)
+            while (c < (uint32_t)P && merge_dsmem[(size_t)tid * P + c] >= bnd) ++c;
+        uint32_t incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += u;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        uint32_t off = incl - c, total = 0;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) {
+            off += w < warp ? wsum[w] : 0u;
+            total += wsum[w];
+        }
+        if (total <= (uint32_t)kLeadCap) { // at least k: the k largest leads
+            for (uint32_t j = 0; j < c; ++j) cand[off + j] = merge_dsmem[(size_t)tid * P + j];
+            __syncthreads();
+            uint64_t *row = &part[0][0][0];
+            for (uint32_t q = tid; q < total; q += kMergeThreads) {
+                const uint64_t x = cand[q];
+                uint32_t rank = 0;
+                for (uint32_t u = 0; u < total; ++u) rank += cand[u] > x;
+                if (rank < (uint32_t)k) row[rank] = x;
+            }
+            __syncthreads();
+            if (tid < k) {
+                const uint64_t x = row[tid];
+                out_idx[(int64_t)r * k + tid] = (int32_t)(~(uint32_t)(x >> 16));
+                out_val[(int64_t)r * k + tid] = (uint16_t)(x & 0xFFFFu);
+            }
+            if (tid == 0) {
+                out_count[r] = k;
+                out_mask[r] = flags;
+            }
+            return;
+        }
+    }
+
+    // Otherwise every entry: per lane group two running lists (two
+    // independent chains), starting empty; list j enters as max with its
+    // reverse, then a sort
     uint64_t x[2][E];
 #pragma unroll
     for (int e = 0; e < E; ++e) x[0][e] = x[1][e] = 0;
@@ -965,8 +1031,6 @@ topk_head_merge_kernel(const uint64_t *__restrict__ ws_entries, const uint64_t *
         a[0][0] = max64(a[0][0], c);
         bitonic_sort_desc<P, 1>(a, lane);
     }
-    f = __reduce_or_sync(0xFFFFFFFFu, f);
-    if (lane == 0 && f) atomicOr(&flags, f);
     if (g == 0) {
 #pragma unroll
         for (int e = 0; e < E; ++e) part[0][warp][i + 32 * e] = a[0][e];
