@@ -64,6 +64,7 @@ constexpr int kRowsN = 16;                    // draft rows, padded (MMA N)
 constexpr int kBoxK = 64;                     // dims per TMA box: one 128-byte swizzle row of bf16
 constexpr int kChunkK = 128;                  // dims per ring stage: two boxes side by side
 constexpr int kStages = 5;                    // TMA ring depth (180 KB in flight)
+constexpr int kPrefetchStages = 2 * kStages;  // weight stages a CTA sends toward L2 before its inputs are ready
 constexpr int kHeadThreads = 352;             // producer warp, MMA warp, eight epilogue warps, helper warp
 constexpr int kEpiThreads = 256;
 constexpr int kEpiWarps = kEpiThreads / 32;
@@ -172,6 +173,12 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     atomicCAS(&g_head_fault, 0u, kFaultWait);
     *abort = 1;
     return false;
+}
+
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int32_t x, int32_t y, uint64_t *bar)
@@ -573,6 +580,20 @@ topk_head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    if (tid == 0) {
+        // while the previous kernel on the stream ends: the weight's first
+        // stages toward L2 (a hint only; L2 is where device memory is
+        // coherent, so a weight that kernel writes is still read after the wait)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_w) : "memory");
+        int n = 0;
+        for (int si = 0; si < nseg && n < kPrefetchStages; ++si) {
+            const Segment g = segment_of(segment_tile(si, u0, u1, nk), u0, u1, nk);
+            for (int kc = g.kc0; kc < g.kc1 && n < kPrefetchStages; ++kc, ++n)
+#pragma unroll
+                for (int bx = 0; bx < kChunkK / kBoxK; ++bx)
+                    tma_prefetch_2d(&tmap_w, kc * kChunkK + bx * kBoxK, (int32_t)(g.tile * kTileM));
+        }
+    }
     grid_dependency_wait(); // the inputs may come from the previous kernel on the stream
 
     volatile uint32_t *abort = &sm.abort;
