@@ -43,7 +43,10 @@ if str(ROOT) not in sys.path:
 
 METRIC = "rows/s and µs/call for bf16 row top-k; achieved HBM GB/s vs GB300 peak"
 DEFAULT_WORKLOAD = "256x248320_k20"
-KERNEL_SOURCE = ROOT / "wide_bf16_row_gb300" / "csrc" / "tf_topk.cu"
+CSRC = ROOT / "wide_bf16_row_gb300" / "csrc"
+KERNEL_SOURCE = CSRC / "tf_topk.cu"
+# the source file each profiled kernel is built from (its hash dates a profile)
+KERNEL_FILES = {"topk_f32_cluster_kernel": CSRC / "tf_topk_f32.cu"}
 PROFILES = ROOT / "profiles"
 # the kernel each launch plan runs (the ncu summaries are named after it)
 PLAN_KERNEL = {1: "topk_stream_kernel_rowwise", 2: "topk_cluster_kernel_S2", 4: "topk_cluster_kernel_S4",
@@ -91,21 +94,20 @@ def measured_peak_hbm() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    return hashlib.sha256(KERNEL_SOURCE.read_bytes()).hexdigest()
+def kernel_source_hash(kernel: str = "") -> str:
+    return hashlib.sha256(KERNEL_FILES.get(kernel, KERNEL_SOURCE).read_bytes()).hexdigest()
 
 
-def profiled_traffic(plan: int, workload: str) -> int | None:
-    """DRAM bytes per launch of the plan's kernel on this workload, from the
-    committed ncu summary, if it was taken on the current kernel source (else
-    None)."""
+def profiled_traffic(kernel: str, workload: str) -> int | None:
+    """DRAM bytes per launch of `kernel` on this workload, from the committed
+    ncu summary, if it was taken on the kernel's current source (else None)."""
     try:
-        text = (PROFILES / f"{PLAN_KERNEL[plan]}_{workload}.md").read_text()
-    except (OSError, KeyError):
+        text = (PROFILES / f"{kernel}_{workload}.md").read_text()
+    except OSError:
         return None
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
-    if not h or not t or h.group(1) != kernel_source_hash():
+    if not h or not t or h.group(1) != kernel_source_hash(kernel):
         return None
     return int(t.group(1))
 
@@ -571,6 +573,9 @@ def run_ours(args) -> None:
     plan = (plan_arg if plan_arg else topk.plan(rows, cols, k)) if fast else 64
     if fmt == "f16" and plan in (1, 32):
         plan = 64
+    # fp32 with k <= 64 on AUTO: the library's fp32 cluster kernel
+    f32_cluster = fmt == "f32" and k <= FAST_MAX_K and plan_arg == 0
+    kernel = "topk_f32_cluster_kernel" if f32_cluster else PLAN_KERNEL.get(plan, "")
     label = run_label(w, fmt, k)
 
     def call(view):
@@ -725,7 +730,7 @@ def run_ours(args) -> None:
             "data": "synthetic",
             "config": workload_config(w, {
                 **({} if label == w.name else {"workload": label, "k": k, "format": fmt}),
-                "plan": PLAN_NAME.get(plan, str(plan)),
+                "plan": "f32_cluster" if f32_cluster else PLAN_NAME.get(plan, str(plan)),
                 "l2": f"inputs rotate over {nbuf} device copies ({nbuf * in_bytes / 1e6:.0f} MB, "
                       f"L2 {l2 / 1e6:.0f} MB)",
                 "parallelism": f"replicas x{world} (rows independent, no exchange)"}),
@@ -736,7 +741,7 @@ def run_ours(args) -> None:
             "us_per_call_l2_warm": warm_us,
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(plan, label),
+                         "frac": achieved / peak, "traffic": profiled_traffic(kernel, label),
                          "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "launches_timed": args.steps,
