@@ -1434,6 +1434,14 @@ __device__ __forceinline__ void load_chunk(uint32_t (&kv)[kVecPerThread][4], con
     }
 }
 
+// n 16-byte vectors from p toward L2 (n <= 0: none); p and the vectors lie
+// inside the caller's rows.
+__device__ __forceinline__ void l2_prefetch_vecs(const uint4 *p, int32_t n)
+{
+    if (n > 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)n * 16u) : "memory");
+}
+
 // grid.x = rows * S; the launch groups each row's S CTAs into one cluster
 // (cluster rank == span).
 template <int S, int kFmt = kBf16>
@@ -1449,15 +1457,21 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     const int span = (int)(blockIdx.x % S);
     const int64_t row = (int64_t)(blockIdx.x / S);
 
-    grid_dependency_wait();
-    cluster_arrive_relaxed(); // paired with the wait before DSMEM use
-
     ChunkGeom geo = row_geometry(logits + row * row_stride, cols);
     const uint4 *vbase = reinterpret_cast<const uint4 *>(geo.rowp - geo.m);
     const int32_t nvec = (cols + geo.m + 7) >> 3;
     const int32_t per_span = (nvec + S - 1) / S;
     const int32_t v_begin = min(nvec, span * per_span);
     const int32_t v_end = min(nvec, v_begin + per_span);
+    // while the previous kernel on the stream ends: the first chunk's whole
+    // vectors toward L2 (a hint only: L2 is where device memory is coherent,
+    // so values that kernel writes are still read after the wait)
+    if (tid == 0) {
+        const int32_t a = max(v_begin, geo.vfull0), e = min(min(v_end, v_begin + kChunkVecs), geo.vfull1);
+        l2_prefetch_vecs(vbase + a, e - a);
+    }
+    grid_dependency_wait();
+    cluster_arrive_relaxed(); // paired with the wait before DSMEM use
 
     if (tid == 0) {
         sm.flags = 0;
@@ -2073,6 +2087,14 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     const int tid = threadIdx.x;
     const int64_t r = blockIdx.x;
     const T *row = logits + r * row_stride;
+    // while the previous kernel on the stream ends: the row's first batch of
+    // whole vectors toward L2 (a hint only: L2 is where device memory is
+    // coherent, so values that kernel writes are still read after the wait)
+    if (tid == 0) {
+        const int32_t h0 = wide_head(row, cols);
+        const int32_t n = min((cols - h0) / (16 / (int)sizeof(T)), kWideUnroll * kWideThreads);
+        l2_prefetch_vecs(reinterpret_cast<const uint4 *>(row + h0), n);
+    }
     // one CTA per row: the next launch is placed as this one's CTAs finish
     // (scheduled early, its CTAs would crowd the SMs still running rows)
     grid_dependency_wait_only();

@@ -383,12 +383,20 @@ topk_f32_cluster_kernel(const uint32_t *__restrict__ logits, int32_t cols, int64
     const int tid = threadIdx.x, lane = tid & 31;
     const int span = (int)(blockIdx.x % S);
     const int64_t row = (int64_t)(blockIdx.x / S);
-    grid_dependency_wait();
-    if constexpr (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-
     const F32Geom g = f32_geometry(logits + row * row_stride, cols);
     const int32_t per = (g.nvec + S - 1) / S;
     const int32_t vb = min(g.nvec, span * per), ve = min(g.nvec, vb + per);
+    // while the previous kernel on the stream ends: the first chunk's whole
+    // vectors toward L2 (a hint only: L2 is where device memory is coherent)
+    if (tid == 0) {
+        const int32_t a = max(vb, g.vfull0), e = min(min(ve, vb + kF32ChunkVecs), g.vfull1);
+        if (e > a)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const uint4 *>(g.rowp - g.m) + a),
+                         "r"((uint32_t)(e - a) * 16u)
+                         : "memory");
+    }
+    grid_dependency_wait();
+    if constexpr (S > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     if (tid == 0) {
         sm.flags = 0;
         sm.n_cand = 0;
