@@ -25,9 +25,9 @@ def nvcc() -> str:
     return cand
 
 
-def compile_command(src: Path, obj: Path) -> list[str]:
+def compile_command(src: Path, obj: Path, defines: tuple[str, ...] = ()) -> list[str]:
     return [nvcc(), "-O3", "-std=c++17", ARCH, "-lineinfo", "-Xcompiler", "-fPIC", "-c",
-            "-I", str(ROOT / "include"), "-o", str(obj), str(src)]
+            *[f"-D{d}" for d in defines], "-I", str(ROOT / "include"), "-o", str(obj), str(src)]
 
 
 def link_command(objs: list[Path], out: Path) -> list[str]:
@@ -44,9 +44,22 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> Path:
     if up_to_date() and not force:
         return LIBRARY
-    tmp = LIBRARY.with_name(f"{LIBRARY.name}.tmp{os.getpid()}")
-    objs = [LIBRARY.with_name(f"{src.stem}.tmp{os.getpid()}.o") for src in SOURCES]
-    cmds = [compile_command(src, obj) for src, obj in zip(SOURCES, objs)]
+    return _build_library(LIBRARY, (), verbose)
+
+
+def build_variant(name: str, defines: tuple[str, ...]) -> Path:
+    """A separate library ``libtf_topk_<name>.so`` compiled with extra macros
+    (test builds, e.g. a forced wait timeout); the product library is untouched."""
+    out = PKG / f"libtf_topk_{name}.so"
+    if out.exists() and all(p.stat().st_mtime <= out.stat().st_mtime for p in SOURCES + HEADERS):
+        return out
+    return _build_library(out, defines, False)
+
+
+def _build_library(library: Path, defines: tuple[str, ...], verbose: bool) -> Path:
+    tmp = library.with_name(f"{library.name}.tmp{os.getpid()}")
+    objs = [library.with_name(f"{library.stem}_{src.stem}.tmp{os.getpid()}.o") for src in SOURCES]
+    cmds = [compile_command(src, obj, defines) for src, obj in zip(SOURCES, objs)]
     if verbose:
         for cmd in cmds:
             print(" ".join(cmd), file=sys.stderr)
@@ -56,12 +69,12 @@ def build(force: bool = False, verbose: bool = False) -> Path:
             for result in pool.map(lambda c: subprocess.run(c, check=True), cmds):
                 pass
         subprocess.run(link_command(objs, tmp), check=True)
-        os.replace(tmp, LIBRARY)
+        os.replace(tmp, library)
     finally:
         for obj in objs:
             if obj.exists():
                 obj.unlink()
-    return LIBRARY
+    return library
 
 
 if __name__ == "__main__":

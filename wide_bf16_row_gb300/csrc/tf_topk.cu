@@ -1002,10 +1002,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Bounded wait: true once the phase with this parity has completed, false
-// after kWaitLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// after `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit)
 {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -1150,8 +1150,16 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
     const int64_t g0 = range_start(b, per, total, nvr);
     const int64_t g1 = range_start(b + 1, per, total, nvr);
 
+#ifdef TF_TOPK_TEST_WAIT_TIMEOUT
+    // test build only: a barrier nothing completes, waited on after the first
+    // chunk has landed, so that the wait runs out and the abort path runs
+    __shared__ uint64_t never_bar;
+#endif
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&sm.mbar[s], 1);
+#ifdef TF_TOPK_TEST_WAIT_TIMEOUT
+        mbar_init(&never_bar, 1);
+#endif
         sm.n_cand = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1245,6 +1253,9 @@ topk_stream_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t ro
             // (and makes the previous chunk's pushes visible)
             bool ok = true;
             if (tid == 0) ok = mbar_wait(&sm.mbar[s], (uint32_t)((c / kStages) & 1));
+#ifdef TF_TOPK_TEST_WAIT_TIMEOUT
+            if (tid == 0 && c == 0) ok = ok && mbar_wait(&never_bar, 0, 64);
+#endif
             if (__syncthreads_or(!ok)) {
                 aborted = true;
                 break;
