@@ -49,7 +49,7 @@ KERNEL_SOURCE = CSRC / "tf_topk.cu"
 KERNEL_FILES = {"topk_f32_cluster_kernel": CSRC / "tf_topk_f32.cu"}
 PROFILES = ROOT / "profiles"
 # the kernel each launch plan runs (the ncu summaries are named after it)
-PLAN_KERNEL = {1: "topk_stream_kernel_rowwise", 2: "topk_cluster_kernel_S2", 4: "topk_cluster_kernel_S4",
+PLAN_KERNEL = {1: "topk_cluster_kernel_S1", 2: "topk_cluster_kernel_S2", 4: "topk_cluster_kernel_S4",
                8: "topk_cluster_kernel_S8", 16: "topk_cluster_kernel_S16", 32: "topk_stream_kernel",
                64: "topk_wide_kernel"}
 PLAN_NAME = {1: "single", 2: "cluster2", 4: "cluster4", 8: "cluster8", 16: "cluster16", 32: "stream", 64: "wide"}
@@ -571,7 +571,7 @@ def run_ours(args) -> None:
     # the wide kernel
     fast = fmt in ("bf16", "f16") and k <= FAST_MAX_K and plan_arg != 64
     plan = (plan_arg if plan_arg else topk.plan(rows, cols, k)) if fast else 64
-    if fmt == "f16" and plan in (1, 32):
+    if fmt == "f16" and plan == 32:
         plan = 64
     # fp32 with k <= 64 on AUTO: the library's fp32 cluster kernel
     f32_cluster = fmt == "f32" and k <= FAST_MAX_K and plan_arg == 0

@@ -100,12 +100,15 @@ int tf_topk_bf16(const void *logits, int64_t rows, int64_t cols, int64_t row_str
                  uint32_t *out_nonfinite_mask, void *stream);
 
 /* Launch plans (tf_topk_bf16_with_plan).  Every plan gives identical results. */
-#define TF_TOPK_PLAN_AUTO 0      /* what tf_topk_bf16 picks for the shape: CLUSTER2 with
-                                    at least one row per SM, else the cluster plan whose
-                                    grid reaches about two CTAs per SM without spans
-                                    narrower than half a chunk (measured on GB300) */
-#define TF_TOPK_PLAN_SINGLE 1    /* control: one CTA streams each whole row (the
-                                    pages' single-group kernel) */
+#define TF_TOPK_PLAN_AUTO 0      /* what tf_topk_bf16 picks for the shape (measured on
+                                    GB300): with at least one row per SM, SINGLE when a
+                                    row is at most one chunk (16384 columns) or when two
+                                    spans a row would take three waves or more, else
+                                    CLUSTER2; with fewer rows, the span count whose grid
+                                    reaches about two CTAs per SM without spans narrower
+                                    than half a chunk (SINGLE when even two would be) */
+#define TF_TOPK_PLAN_SINGLE 1    /* one CTA per whole row (the pages' single-group
+                                    kernel): the cluster kernel without a split */
 #define TF_TOPK_PLAN_CLUSTER2 2  /* each row split into 2/4/8/16 column spans, one */
 #define TF_TOPK_PLAN_CLUSTER4 4  /*   CTA each, inside one thread-block cluster; */
 #define TF_TOPK_PLAN_CLUSTER8 8  /*   the span lists are merged through distributed */
@@ -275,14 +278,15 @@ int tf_topk_nucleus_bf16(const uint16_t *val, const int32_t *count, int64_t rows
  *                out_nonfinite_mask uint32 [rows] (1 NaN, 2 +inf, 4 -inf).
  * bf16 with k <= TF_TOPK_MAX_K runs the plans of tf_topk_bf16 (the same
  * results, byte for byte).  fp16 with k <= TF_TOPK_MAX_K runs the cluster
- * plans (it shares bf16's order-preserving key map; only its special values
- * differ), except where AUTO would give a row one CTA.  fp32 with k <=
+ * kernel's plans, SINGLE and CLUSTER2..16 (it shares bf16's order-preserving
+ * key map; only its special values differ).  fp32 with k <=
  * TF_TOPK_MAX_K on AUTO runs the fp32 cluster kernel: each row's column spans
  * over a thread-block cluster, read once against a running bound, on 32-bit
  * keys.  Everything else (and TF_TOPK_PLAN_WIDE) runs the wide kernel: one
- * CTA per row, two passes over the row (a bound from each thread's best keys,
- * then every element reaching it, ranked), with an exact counting search when
- * ties crowd the bound.  Asynchronous on `stream`; allocates nothing.
+ * CTA per row, two passes over the row (a bound from each thread's largest
+ * vector maxima, then every element reaching it, read back through a table of
+ * the maxima and ranked or sorted), with an exact counting search when ties
+ * crowd the bound.  Asynchronous on `stream`; allocates nothing.
  * Returns a TF_TOPK_* status: ERR_DTYPE for an unknown format, ERR_K,
  * ERR_SHAPE, ERR_NULL, ERR_ALIGN as for tf_topk_bf16.
  */
@@ -296,8 +300,9 @@ int tf_topk_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols
                    int32_t *out_idx, void *out_val, int32_t *out_count, uint32_t *out_nonfinite_mask, void *stream);
 
 /* tf_topk_select with a plan: TF_TOPK_PLAN_AUTO, TF_TOPK_PLAN_WIDE, or, with
- * k <= TF_TOPK_MAX_K, a plan of tf_topk_bf16_with_plan (bf16) or a cluster
- * plan CLUSTER2..16 (fp16); anything else returns TF_TOPK_ERR_PLAN. */
+ * k <= TF_TOPK_MAX_K, a plan of tf_topk_bf16_with_plan (bf16) or SINGLE and
+ * the cluster plans CLUSTER2..16 (fp16); anything else returns
+ * TF_TOPK_ERR_PLAN. */
 int tf_topk_select_with_plan(const void *logits, int32_t dtype, int64_t rows, int64_t cols, int64_t row_stride,
                              int32_t k, int32_t *out_idx, void *out_val, int32_t *out_count,
                              uint32_t *out_nonfinite_mask, int32_t plan, void *stream);

@@ -182,7 +182,7 @@ def select_call(lib, dtype=0, rows=4, cols=100, stride=100, k=8, logits=FAKE, id
     (dict(dtype=3), 10), (dict(dtype=-1), 10),
     (dict(k=0), 3), (dict(k=1025), 3), (dict(dtype=2, k=1025), 3),
     (dict(rows=-1), 2), (dict(cols=0), 2), (dict(stride=99), 2),
-    (dict(dtype=1, plan=1), 5), (dict(dtype=1, plan=32), 5), (dict(dtype=1, k=65, plan=2), 5),
+    (dict(dtype=1, plan=32), 5), (dict(dtype=1, k=65, plan=2), 5), (dict(dtype=1, k=65, plan=1), 5),
     (dict(k=65, plan=2), 5), (dict(plan=3), 5), (dict(dtype=2, plan=32), 5), (dict(dtype=2, plan=2), 5),
     (dict(logits=None), 1), (dict(idx=None), 1), (dict(val=None), 1), (dict(count=None), 1), (dict(mask=None), 1),
     (dict(logits=FAKE + 1), 4), (dict(dtype=2, logits=FAKE + 2), 4), (dict(dtype=2, val=FAKE + 2), 4),

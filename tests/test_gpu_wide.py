@@ -155,9 +155,9 @@ def test_bf16_small_k_matches_tf_topk_bf16():
         assert_same(got, gpu_topk(w.logits, w.cols, w.k, plan=plan), f"select plan {plan}")
 
 
-@pytest.mark.parametrize("plan", [0, 2, 4, 8, 16])
+@pytest.mark.parametrize("plan", [0, 1, 2, 4, 8, 16])
 def test_f16_on_the_cluster_plans(plan):
-    """fp16, k <= 64, on CLUSTER2..16 (and AUTO): mixed rows with every fp16
+    """fp16, k <= 64, on SINGLE and CLUSTER2..16 (and AUTO): mixed rows with every fp16
     special, padded strides, an unaligned row base, heavy ties (the exact
     path) and all-NaN rows, against the oracle."""
     x = gen("f16", 6, 70001, 3 + plan, 70016, special_frac=0.02, dup_frac=0.05)

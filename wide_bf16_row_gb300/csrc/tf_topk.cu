@@ -103,6 +103,7 @@ constexpr int kMaxSpans = TF_TOPK_MAX_SPANS;
 constexpr int kCandCap = 256;        // candidates ranked directly (one per thread)
 constexpr int kStages = 3;           // TMA ring depth of the stream kernel
 constexpr int kStreamCtasPerSm = 2;  // resident stream CTAs per SM
+constexpr int kClusterCtasPerSm = 4; // resident cluster-kernel CTAs per SM (its launch bounds)
 constexpr int kMinVecsPerCta = 1024; // smallest range a stream CTA is given
 constexpr int kMaxPieces = kMaxSpans;// most pieces a stream row is cut into
 constexpr uint32_t kWaitLimit = 1u << 22;
@@ -1456,7 +1457,7 @@ __device__ __forceinline__ void l2_prefetch_vecs(const uint4 *p, int32_t n)
 // grid.x = rows * S; the launch groups each row's S CTAs into one cluster
 // (cluster rank == span).
 template <int S, int kFmt = kBf16>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, kClusterCtasPerSm)
 topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
                     int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
                     int32_t *__restrict__ out_count, uint32_t *__restrict__ out_mask)
@@ -2578,40 +2579,41 @@ int validate(const void *logits, int64_t rows, int64_t cols, int64_t row_stride,
 int32_t vectors_per_row(int64_t cols) { return (int32_t)((cols + 14) >> 3); }
 
 // Stream-plan geometry: the range each CTA gets, and the CTA count.
-void stream_geometry(int64_t rows, int64_t cols, int sm_count, bool one_row_per_cta, int64_t *per_out,
-                     int64_t *ctas_out)
+void stream_geometry(int64_t rows, int64_t cols, int sm_count, int64_t *per_out, int64_t *ctas_out)
 {
     const int64_t nvr = vectors_per_row(cols);
     const int64_t total = rows * nvr;
-    int64_t per;
-    if (one_row_per_cta) {
-        per = nvr;
-    } else {
-        const int64_t slots = (int64_t)sm_count * kStreamCtasPerSm;
-        per = (total + slots - 1) / slots;
-        per = per < kMinVecsPerCta ? kMinVecsPerCta : per;
-        // a row meets <= kMaxPieces CTAs, after range starts move by up to 2 * kThreads
-        const int64_t min_piece = (nvr + kMaxPieces - 2) / (kMaxPieces - 1) + 2 * kThreads;
-        per = per < min_piece ? min_piece : per;
-    }
+    const int64_t slots = (int64_t)sm_count * kStreamCtasPerSm;
+    int64_t per = (total + slots - 1) / slots;
+    per = per < kMinVecsPerCta ? kMinVecsPerCta : per;
+    // a row meets <= kMaxPieces CTAs, after range starts move by up to 2 * kThreads
+    const int64_t min_piece = (nvr + kMaxPieces - 2) / (kMaxPieces - 1) + 2 * kThreads;
+    per = per < min_piece ? min_piece : per;
     *per_out = per;
     *ctas_out = (total + per - 1) / per;
 }
 
-// The plan tf_topk_bf16 uses.  Measured on GB300 over widths 4096..248320,
-// rows 1..1024 and every plan: the cluster plans are the fastest, or within
-// noise of it, everywhere.  With at least one row per SM two spans per row win;
-// with fewer rows, the span count that brings the grid to about two CTAs per
-// SM, but no span narrower than half a chunk (a whole chunk for k > 32, whose
-// merges cost more).
+// The plan tf_topk_bf16 uses.  Measured on GB300 over widths 4096..248320
+// and rows 1..2048: the cluster kernel is the fastest everywhere.  With at
+// least one row per SM, one CTA per row (SINGLE) when a row is at most one
+// chunk, or when two spans a row would take three waves or more of the
+// kernel's four CTAs an SM (1024 x 248320: 88.0 -> 83.1 us; 1024 x 4096:
+// 25.6 -> 13.8 us); else two spans a row.  With fewer rows, the span count
+// that brings the grid to about two CTAs per SM, but no span narrower than
+// half a chunk (a whole chunk for k > 32, whose merges cost more), down to
+// one span.
 int32_t pick_plan(int64_t rows, int64_t cols, int32_t k, int sm_count)
 {
-    if (rows >= sm_count) return TF_TOPK_PLAN_CLUSTER2;
+    if (rows >= sm_count) {
+        const int64_t slots = (int64_t)kClusterCtasPerSm * sm_count;
+        if (cols <= kChunkCols || 2 * rows >= 3 * slots) return TF_TOPK_PLAN_SINGLE;
+        return TF_TOPK_PLAN_CLUSTER2;
+    }
     const int64_t min_span = k > 32 ? kChunkCols : kChunkCols / 2;
     int s = 2;
     while (s < kMaxSpans && rows * s < 2 * (int64_t)sm_count) s *= 2;
-    while (s > 2 && cols / s < min_span) s /= 2;
-    return s;
+    while (s > 1 && cols / s < min_span) s /= 2;
+    return s == 1 ? TF_TOPK_PLAN_SINGLE : s;
 }
 
 template <int S, int kFmt = kBf16>
@@ -2646,28 +2648,22 @@ cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, i
 
 int launch_stream(int dev, int sm_count, const uint16_t *logits, int64_t rows, int64_t cols,
                   int64_t row_stride, int32_t k, int32_t *out_idx, uint16_t *out_val, int32_t *out_count,
-                  uint32_t *out_mask, bool one_row_per_cta, cudaStream_t stream)
+                  uint32_t *out_mask, cudaStream_t stream)
 {
     const int32_t nvr = vectors_per_row(cols);
-    // one launch covers at most 2^31-1 CTAs; longer matrices go in row blocks
-    const int64_t rows_per_launch = one_row_per_cta ? (int64_t)INT32_MAX : rows;
-    for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
-        const int64_t nr = rows - r0 < rows_per_launch ? rows - r0 : rows_per_launch;
+    {
+        const int64_t r0 = 0, nr = rows;
         int64_t per = 0, ctas = 0;
-        stream_geometry(nr, cols, sm_count, one_row_per_cta, &per, &ctas);
-        uint64_t *partials = nullptr;
-        uint32_t *tickets = nullptr;
-        if (!one_row_per_cta) {
-            Scratch *s = nullptr;
-            const int st = get_scratch(dev, stream, ctas, &s);
-            if (st != TF_TOPK_OK) return st;
-            partials = s->partials;
-            tickets = s->tickets;
-            // a launch whose wait ran out leaves its split rows' tickets half
-            // counted: start every launch from zero
-            const cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)ctas * sizeof(uint32_t), stream);
-            if (e != cudaSuccess) return fail_cuda(e);
-        }
+        stream_geometry(nr, cols, sm_count, &per, &ctas);
+        Scratch *sc = nullptr;
+        const int st = get_scratch(dev, stream, ctas, &sc);
+        if (st != TF_TOPK_OK) return st;
+        uint64_t *partials = sc->partials;
+        uint32_t *tickets = sc->tickets;
+        // a launch whose wait ran out leaves its split rows' tickets half
+        // counted: start every launch from zero
+        const cudaError_t em = cudaMemsetAsync(tickets, 0, (size_t)ctas * sizeof(uint32_t), stream);
+        if (em != cudaSuccess) return fail_cuda(em);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)ctas, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
@@ -2707,11 +2703,10 @@ int run(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int3
     cudaError_t e = cudaSuccess;
     switch (plan) {
     case TF_TOPK_PLAN_SINGLE:
-        return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
-                             true, s);
+        e = launch_cluster<1>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        break;
     case TF_TOPK_PLAN_STREAM:
-        return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask,
-                             false, s);
+        return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask, s);
     case TF_TOPK_PLAN_CLUSTER2:
         e = launch_cluster<2>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
         break;
@@ -2759,7 +2754,7 @@ int run_noalloc(const void *logits, int64_t rows, int64_t cols, int64_t row_stri
     st = device_setup(&dev, &sm_count);
     if (st != TF_TOPK_OK) return st;
     int64_t per = 0, ctas = 0;
-    stream_geometry(rows, cols, sm_count, false, &per, &ctas);
+    stream_geometry(rows, cols, sm_count, &per, &ctas);
     if (ctas > TF_TOPK_NOALLOC_MAX_CTAS) return TF_TOPK_ERR_SCRATCH;
     uint64_t *base = nullptr;
     st = noalloc_scratch(dev, &base);
@@ -2934,11 +2929,12 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
     if (k < 1 || k > kWideMaxK) return TF_TOPK_ERR_K;
     if (rows < 0 || cols < 1 || row_stride < cols || cols > (int64_t)INT32_MAX - 64) return TF_TOPK_ERR_SHAPE;
     if (rows > 0 && row_stride > INT64_MAX / rows) return TF_TOPK_ERR_SHAPE;
-    const bool cluster_plan = plan == TF_TOPK_PLAN_CLUSTER2 || plan == TF_TOPK_PLAN_CLUSTER4 ||
-                              plan == TF_TOPK_PLAN_CLUSTER8 || plan == TF_TOPK_PLAN_CLUSTER16;
+    const bool cluster_plan = plan == TF_TOPK_PLAN_SINGLE || plan == TF_TOPK_PLAN_CLUSTER2 ||
+                              plan == TF_TOPK_PLAN_CLUSTER4 || plan == TF_TOPK_PLAN_CLUSTER8 ||
+                              plan == TF_TOPK_PLAN_CLUSTER16;
     if (plan != TF_TOPK_PLAN_AUTO && plan != TF_TOPK_PLAN_WIDE &&
         !(k <= kMaxK && (dtype == TF_TOPK_DTYPE_BF16 || (dtype == TF_TOPK_DTYPE_F16 && cluster_plan))))
-        return TF_TOPK_ERR_PLAN; // bf16: every plan; fp16: the cluster plans; both with k <= 64
+        return TF_TOPK_ERR_PLAN; // bf16: every plan; fp16: SINGLE and the cluster plans; both with k <= 64
     if (rows == 0) return TF_TOPK_OK;
     if (!logits || !out_idx || !out_val || !out_count || !out_mask) return TF_TOPK_ERR_NULL;
     const uintptr_t esz = dtype == TF_TOPK_DTYPE_F32 ? 4 : 2;
@@ -2964,6 +2960,9 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
         const int32_t c = (int32_t)cols;
         cudaError_t e = cudaSuccess;
         switch (p) {
+        case TF_TOPK_PLAN_SINGLE:
+            e = launch_cluster<1, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            break;
         case TF_TOPK_PLAN_CLUSTER2:
             e = launch_cluster<2, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
             break;
@@ -2977,7 +2976,7 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
             e = launch_cluster<16, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask,
                                                       s);
             break;
-        default: // narrow rows, where AUTO would take one CTA per row: the wide kernel
+        default: // not reached (AUTO and the accepted plans are above): the wide kernel
             p = TF_TOPK_PLAN_WIDE;
             break;
         }
