@@ -187,8 +187,10 @@ def test_f16_bench_shape_auto():
 
 
 # fp32 with k <= 64 on AUTO runs the fp32 cluster kernel; the shapes pick its
-# span counts 1, 2, 4 and 8 (one row per SM or more: 2)
-F32_SHAPES = [(6, 5000, 5008), (3, 70001, 70016), (40, 40000, 40000), (160, 20000, 20004)]
+# span counts 1 (few rows; a row per SM or more with rows of one chunk; many
+# rows), 2, 4 and 8
+F32_SHAPES = [(6, 5000, 5008), (3, 70001, 70016), (40, 40000, 40000), (160, 20000, 20004), (200, 8000, 8004),
+              (1000, 3000, 3001)]
 
 
 @pytest.mark.parametrize("rows,cols,stride", F32_SHAPES, ids=lambda v: str(v))

@@ -435,26 +435,29 @@ topk_f32_cluster_kernel(const uint32_t *__restrict__ logits, int32_t cols, int64
         }
         // the registers are free: the next chunk's loads fly from here on
         if (ce < ve) f32_load_chunk(kv, g, ce, ve);
-        // slots: a warp scan of the counts and one atomic a warp
-        uint32_t incl = c;
+        // slots: a warp scan of the counts and one atomic a warp (warps
+        // without a candidate skip it)
+        if (__any_sync(0xFFFFFFFFu, c != 0)) {
+            uint32_t incl = c;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-            if (lane >= d) incl += u;
-        }
-        uint32_t wbase = 0;
-        if (lane == 31 && incl) wbase = atomicAdd(&sm.n_cand, incl);
-        uint32_t slot = __shfl_sync(0xFFFFFFFFu, wbase, 31) + incl - c - cand_base;
-        if (c != 0) {
-            for (int i = 0; i < kF32Vec; ++i) {
-                const uint4 q = sm.stage[i * kF32Threads + tid];
-                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-                const int32_t col = (cb + i * kF32Threads + tid) * 4 - g.m;
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += u;
+            }
+            uint32_t wbase = 0;
+            if (lane == 31) wbase = atomicAdd(&sm.n_cand, incl);
+            uint32_t slot = __shfl_sync(0xFFFFFFFFu, wbase, 31) + incl - c - cand_base;
+            if (c != 0) {
+                for (int i = 0; i < kF32Vec; ++i) {
+                    const uint4 q = sm.stage[i * kF32Threads + tid];
+                    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                    const int32_t col = (cb + i * kF32Threads + tid) * 4 - g.m;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (w4[j] >= uf) {
-                        if (slot < (uint32_t)kF32Cap) sm.cand[slot] = f32_entry(fold0(w4[j]), col + j);
-                        ++slot;
+                    for (int j = 0; j < 4; ++j) {
+                        if (w4[j] >= uf) {
+                            if (slot < (uint32_t)kF32Cap) sm.cand[slot] = f32_entry(fold0(w4[j]), col + j);
+                            ++slot;
+                        }
                     }
                 }
             }
@@ -611,7 +614,12 @@ cudaError_t launch_f32(const uint32_t *x, int64_t rows, int32_t cols, int64_t st
 // that brings the grid to about two CTAs an SM, no span shorter than a chunk.
 int f32_spans(int64_t rows, int64_t cols, int sm_count)
 {
-    if (rows >= sm_count) return 2;
+    // with a row per SM or more: one CTA per row when a row is at most one
+    // chunk, or when two spans a row would take three waves or more of the
+    // kernel's four CTAs an SM (1024 x 248320: 161.4 -> 148.7 us;
+    // 1024 x 8192: 33.4 -> 13.5 us); else two spans
+    if (rows >= sm_count)
+        return (cols <= (int64_t)kF32ChunkVecs * 4 || 2 * rows >= 3 * 4 * (int64_t)sm_count) ? 1 : 2;
     int s = 1;
     while (s < kF32MaxSpans && rows * s * 2 < 2 * (int64_t)sm_count && cols / (2 * s) >= kF32ChunkVecs * 4) s <<= 1;
     return s;
