@@ -170,8 +170,33 @@ def test_gpu_guard_errors_leave_outputs_untouched():
 
 
 def test_plan_table():
+    """AUTO's choice follows the documented rule (4 cluster-kernel CTAs an SM,
+    16384-column chunks): with a row per SM or more, one CTA per row (SINGLE)
+    for rows of at most one chunk or when two spans a row would take three
+    waves or more, else CLUSTER2; with fewer rows, the span count that brings
+    the grid to about two CTAs per SM without spans under half a chunk (a
+    chunk for k > 32), down to one."""
+    import torch
+
     from wide_bf16_row_gb300 import topk
 
-    for rows, cols in ((1, 100), (1, 4096), (15, 98592), (16, 248320), (256, 248320), (1024, 248320)):
-        assert topk.plan(rows, cols, 20) in ALL_PLANS
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunk = 16384
+
+    def rule(rows, cols, k):
+        if rows >= sms:
+            return 1 if (cols <= chunk or 2 * rows >= 3 * 4 * sms) else 2
+        s = 2
+        while s < 16 and rows * s < 2 * sms:
+            s *= 2
+        while s > 1 and cols // s < (chunk if k > 32 else chunk // 2):
+            s //= 2
+        return s
+
+    for rows, cols in ((1, 100), (1, 4096), (15, 98592), (16, 248320), (256, 248320), (1024, 248320),
+                       (1024, 4096), (512, 8192), (640, 248320), (sms, chunk), (sms, chunk + 1), (4, 98592)):
+        for k in (8, 20, 64):
+            got = topk.plan(rows, cols, k)
+            assert got in ALL_PLANS and got == rule(rows, cols, k), (rows, cols, k, got)
+    assert topk.plan(256, 248320, 20) == 2 and topk.plan(15, 98592, 16) == 8
     assert topk.device_fault() == 0
