@@ -1852,7 +1852,8 @@ __device__ __forceinline__ void wide_scan2(const T *row, int32_t cols, Fe &&f, F
         for (int32_t c = tid; c < head; c += kWideThreads) f(c, (uint32_t)row[c]);
     const int32_t nvec = (cols - head) / kPer;
     const uint4 *v = reinterpret_cast<const uint4 *>(row + head);
-    // the last batch too is issued whole (its loads guarded), not one by one
+    // whole batches of kWideUnroll loads, then the rest one by one (a guarded
+    // last batch here cost the exact paths' counting scans spills)
     int32_t i = tid;
     for (; i + (kWideUnroll - 1) * kWideThreads < nvec; i += kWideUnroll * kWideThreads) {
         uint4 q[kWideUnroll];

@@ -856,12 +856,13 @@ static_assert((size_t)kMaxGrid * kMaxK * sizeof(uint64_t) <= kMergeSmemBytes, "a
 // k rounded up to a power of two, at least 2).  Entries are distinct (each
 // holds its column) and the entry order is the row order (score descending,
 // lower column first), so the row's top k are the k largest entries of the
-// union, and a zero (an empty slot) sorts below every entry.  The union's
-// top P comes from pairwise merges: for sorted A and B, max(A[i], B[P-1-i])
-// holds the top P of both and is bitonic, so half-cleaners sort it
-// (Batcher's bitonic merge).  A CTA never contributes more than k entries to
-// the row and its list keeps its best k, so nothing the row needs was left
-// out.
+// union, and a zero (an empty slot) sorts below every entry.  A CTA never
+// contributes more than k entries to the row and its list keeps its best k,
+// so nothing the row needs was left out.  Usually the k-th largest list head
+// bounds the row's top k from below, and the few entries at or above it are
+// ranked directly.  Otherwise the union's top P comes from pairwise merges:
+// for sorted A and B, max(A[i], B[P-1-i]) holds the top P of both and is
+// bitonic, so half-cleaners sort it (Batcher's bitonic merge).
 //
 // A warp holds P-entry lists in registers: for P <= 32 a group of P lanes
 // holds one (entry i in lane i of the group, 32 / P groups side by side); for
