@@ -109,6 +109,33 @@ def constants() -> dict:
 MAX_K = 64
 
 
+_raw_stream = None
+
+
+def _stream_handle(stream, dev) -> int:
+    """The cudaStream_t of ``stream``, or of the current stream of ``dev``
+    (read through torch's raw-stream query where it has one: a plain
+    ``torch.cuda.current_stream`` costs microseconds a call)."""
+    global _raw_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is None:
+        import torch
+        f = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _raw_stream = f if f is not None else (lambda i: torch.cuda.current_stream(i).cuda_stream)
+    return _raw_stream(dev.index)
+
+
+def _on_device(dev, fn, *args):
+    """fn(*args) with ``dev`` the current CUDA device (the library launches on
+    the current device); the device is switched only when it is not already."""
+    import torch
+    if torch.cuda.current_device() == dev.index:
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
 def _check(status: int) -> None:
     if status != OK:
         msg = strerror(status)
@@ -173,11 +200,9 @@ def merge_bf16(idx, val, count, mask, offsets, k: int, *, out=None, stream=None)
                torch.empty((rows, k), dtype=val.dtype, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev))
-    if stream is None:
-        stream = torch.cuda.current_stream(idx.device)
-    _check(tf_topk_merge_bf16(idx.data_ptr(), val.data_ptr(), count.data_ptr(), mask.data_ptr(), rows, shards,
-                              k_in, list(offsets), k, out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
-                              out[3].data_ptr(), stream.cuda_stream))
+    _check(_on_device(idx.device, tf_topk_merge_bf16, idx.data_ptr(), val.data_ptr(), count.data_ptr(),
+                      mask.data_ptr(), rows, shards, k_in, list(offsets), k, out[0].data_ptr(), out[1].data_ptr(),
+                      out[2].data_ptr(), out[3].data_ptr(), _stream_handle(stream, idx.device)))
     return out
 
 
@@ -227,10 +252,9 @@ def nucleus(val, count, temperature: float, top_p: float, *, dtype: int | None =
     if out is None:
         out = (torch.empty((rows, k), dtype=torch.float32, device=val.device),
                torch.empty((rows,), dtype=torch.int32, device=val.device))
-    if stream is None:
-        stream = torch.cuda.current_stream(val.device)
-    _check(tf_topk_nucleus(val.data_ptr(), dtype, count.data_ptr(), rows, k, float(temperature), float(top_p),
-                           out[0].data_ptr(), out[1].data_ptr(), stream.cuda_stream))
+    _check(_on_device(val.device, tf_topk_nucleus, val.data_ptr(), dtype, count.data_ptr(), rows, k,
+                      float(temperature), float(top_p), out[0].data_ptr(), out[1].data_ptr(),
+                      _stream_handle(stream, val.device)))
     return out
 
 
@@ -280,11 +304,9 @@ def select_topk(x, k: int, *, dtype: int | None = None, plan: int = 0, out=None,
                torch.empty((rows, k), dtype=x.dtype, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev))
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
-    _check(tf_topk_select_with_plan(x.data_ptr(), dtype, rows, cols, row_stride, k, out[0].data_ptr(),
-                                    out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(), plan,
-                                    stream.cuda_stream))
+    _check(_on_device(dev, tf_topk_select_with_plan, x.data_ptr(), dtype, rows, cols, row_stride, k,
+                      out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(), out[3].data_ptr(), plan,
+                      _stream_handle(stream, dev)))
     return out
 
 
@@ -332,16 +354,12 @@ def head_topk_bf16(hidden, weight, k: int, *, out=None, workspace=None, stream=N
                torch.empty((rows, k), dtype=torch.bfloat16, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev),
                torch.empty((rows,), dtype=torch.int32, device=dev))
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
-    with torch.cuda.device(dev):
-        if workspace is None:
-            need = tf_topk_head_bf16_workspace(rows, k) if 1 <= rows <= HEAD_MAX_ROWS else 0
-            workspace = torch.empty((max(need, 8),), dtype=torch.uint8, device=dev)
-        status = tf_topk_head_bf16(hidden.data_ptr(), weight.data_ptr(), rows, dim, vocab, k,
-                                   workspace.data_ptr(), workspace.numel(), out[0].data_ptr(), out[1].data_ptr(),
-                                   out[2].data_ptr(), out[3].data_ptr(), stream.cuda_stream)
-    _check(status)
+    if workspace is None:
+        need = _on_device(dev, tf_topk_head_bf16_workspace, rows, k) if 1 <= rows <= HEAD_MAX_ROWS else 0
+        workspace = torch.empty((max(need, 8),), dtype=torch.uint8, device=dev)
+    _check(_on_device(dev, tf_topk_head_bf16, hidden.data_ptr(), weight.data_ptr(), rows, dim, vocab, k,
+                      workspace.data_ptr(), workspace.numel(), out[0].data_ptr(), out[1].data_ptr(),
+                      out[2].data_ptr(), out[3].data_ptr(), _stream_handle(stream, dev)))
     return out
 
 
@@ -404,11 +422,7 @@ def topk_bf16(x, k: int, *, plan: int = 0, out=None, stream=None):
                     or t.device != dev:
                 raise ValueError("out tensors must be contiguous, on x's device, with shapes "
                                  "(rows,k), (rows,k), (rows,), (rows,)")
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
-    with torch.cuda.device(dev):
-        status = tf_topk_bf16_with_plan(x.data_ptr(), rows, cols, row_stride, k, idx.data_ptr(),
-                                        val.data_ptr(), count.data_ptr(), mask.data_ptr(), plan,
-                                        stream.cuda_stream)
-    _check(status)
+    _check(_on_device(dev, library().tf_topk_bf16_with_plan, x.data_ptr(), rows, cols, row_stride, k,
+                      idx.data_ptr(), val.data_ptr(), count.data_ptr(), mask.data_ptr(), plan,
+                      _stream_handle(stream, dev)))
     return idx, val, count, mask
