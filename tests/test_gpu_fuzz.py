@@ -87,3 +87,27 @@ def test_random_case(case):
 def test_no_fault_after_fuzz():
     from wide_bf16_row_gb300 import topk
     assert topk.device_fault() == 0
+
+
+HEAD_CASES = int(os.environ.get("FUZZ_HEAD_CASES", "16"))
+
+
+@pytest.mark.parametrize("case", range(HEAD_CASES))
+def test_random_head_case(case):
+    """The fused draft head on random shapes: rows 1..16, dims of any multiple
+    of 8 up to 640, vocabularies around the tile and grid sizes, k 1..64."""
+    import torch
+
+    from oracle import head as head_oracle
+    from tests.test_gpu_head import _dev, _np
+    from wide_bf16_row_gb300 import synth, topk
+
+    rng = np.random.default_rng([SEED, 1000 + case])
+    rows = int(rng.integers(1, 17))
+    dim = 8 * int(rng.integers(1, 81))
+    vocab = int(rng.choice([int(rng.integers(1, 2000)), int(rng.integers(2000, 40000)),
+                            128 * int(rng.integers(140, 170)) + int(rng.integers(-3, 4))]))
+    k = int(rng.integers(1, 65))
+    h = synth.head_inputs(rows, dim, vocab, k, seed=SEED % 100000 + case)
+    got = _np(topk.head_topk_bf16(_dev(h.hidden).view(torch.bfloat16), _dev(h.weight).view(torch.bfloat16), k))
+    assert_same(got, head_oracle.topk(h.hidden, h.weight, k), f"head fuzz case {case}: {rows}x{dim}x{vocab} k {k}")
