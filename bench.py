@@ -246,12 +246,14 @@ def isolated_launches(step, stream, dev, n: int) -> list[float]:
     return out
 
 
-# The workloads the per-config table covers: the four named ones and sweep points.
+# The workloads the per-config table covers: the four named ones, the widest
+# of them with a -inf mask, and sweep points.
 PER_CONFIG = (
     ("1x4096_k8", None),
     ("15x98592_k16", None),
     ("16x248320_k64_specials", None),
     ("256x248320_k20", None),
+    ("256x248320_k20_masked", None),
     ("sweep_1024x248320_k20", (248320, 1024, 20)),
     ("sweep_64x151936_k64", (151936, 64, 64)),
     ("sweep_4x98592_k8", (98592, 4, 8)),
@@ -262,7 +264,9 @@ PER_CONFIG = (
 def per_config_workload(name: str, sweep):
     from wide_bf16_row_gb300 import synth
 
-    return synth.config_sweep(*sweep) if sweep else synth.NAMED[name]()
+    if sweep:
+        return synth.config_sweep(*sweep)
+    return synth.config_masked_window() if name.endswith("_masked") else synth.NAMED[name]()
 
 
 def measure_config(w, dev, peak: float, cpu: bool, cpu_seconds: float) -> dict:

@@ -101,6 +101,33 @@ def test_heavy_ties_and_nan(cols, k):
         assert_same(gpu_topk(x, cols, k, plan=plan), exp, f"ties cols={cols} k={k} plan={plan}")
 
 
+MASKS = ((0.1, 0, 0.0), (0.6, 0, 0.0), (0.0, 1000, 0.0), (0.1, 64, 0.0005))
+
+
+@pytest.mark.parametrize("rows,cols,k", [(256, 248320, 20), (16, 248320, 64), (15, 98592, 16), (1024, 4096, 8)])
+def test_masked_rows(rows, cols, k):
+    """-inf masks (random, dense, a padded vocabulary's tail) with a few +inf:
+    chunks whose only non-finite values are infinities keep their keys and
+    only record the flags."""
+    for i, (frac, tail, pinf) in enumerate(MASKS):
+        x = synth.masked_rows(rows, cols, seed=cols + i, mask_frac=frac, tail=tail, plus_inf_frac=pinf,
+                              row_stride=cols + (8 if i % 2 else 0))
+        exp = oracle.topk(x, cols, k)
+        for plan in (0, 1, 2, 8, 32):
+            assert_same(gpu_topk(x, cols, k, plan=plan, offset=i), exp,
+                        f"masked {rows}x{cols} k={k} mask={frac} tail={tail} +inf={pinf} plan={plan}")
+
+
+def test_masked_rows_f16():
+    from tests.test_gpu_wide import gpu_select
+
+    for i, (frac, tail, pinf) in enumerate(MASKS):
+        x = synth.masked_rows(24, 98592, seed=7 + i, mask_frac=frac, tail=tail, plus_inf_frac=pinf, fmt="f16")
+        exp = oracle.topk(x, 98592, 16, dtype="f16")
+        for plan in (0, 1, 8):
+            assert_same(gpu_select(x, 98592, 16, "f16", plan=plan), exp, f"f16 masked mask={frac} plan={plan}")
+
+
 def test_every_plan_agrees_on_random_rows():
     x = synth.mixed_rows(40, 70000, seed=99, row_stride=70003, special_frac=0.002, dup_frac=0.01)
     exp = oracle.topk(x, 70000, 37)

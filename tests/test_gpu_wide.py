@@ -146,6 +146,23 @@ def test_specials_config_all_formats():
                         f"{dtype} 248320 k{k}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_masked_rows_all_formats(dtype):
+    """-inf masks (random, dense, a padded vocabulary's tail) with a few +inf,
+    no NaN, through AUTO and the wide kernel: vectors whose only non-finite
+    values are infinities skip the exact re-scan and keep their keys."""
+    masks = ((0.1, 0, 0.0), (0.6, 0, 0.0), (0.0, 3000, 0.0), (0.1, 64, 0.0005))
+    for i, (frac, tail, pinf) in enumerate(masks):
+        cols = 70001 if i % 2 else 98592
+        x = synth.masked_rows(24, cols, seed=31 + i, mask_frac=frac, tail=tail, plus_inf_frac=pinf,
+                              row_stride=cols + 3 * (i % 2), fmt=dtype)
+        for k in (20, 300, 1024):
+            exp = oracle.topk(x, cols, k, dtype=dtype)
+            for plan in (0, 64):
+                assert_same(gpu_select(x, cols, k, dtype, plan=plan, offset=i % 3), exp,
+                            f"{dtype} masked mask={frac} tail={tail} +inf={pinf} k{k} plan{plan}")
+
+
 def test_bf16_small_k_matches_tf_topk_bf16():
     """tf_topk_select on bf16 with k <= 64 runs the tf_topk_bf16 plans: same bytes."""
     from tests.gpu_util import gpu_topk

@@ -293,8 +293,28 @@ def pin_f16_f32_argsort(oracle: Oracle) -> None:
             check_against(oracle, x, cols, k, reference_rows(x, cols, k, dtype), dtype=dtype)
 
 
+def pin_masked_rows(oracle: Oracle) -> None:
+    """-inf masks (random, dense, a padded vocabulary's tail, every column)
+    with a few +inf in each format: -inf is a number that sorts last and sets
+    mask bit 4 (+inf bit 2); numpy's stable argsort of -value decides."""
+    for dtype in ("bf16", "f16", "f32"):
+        for seed, (frac, tail, pinf, k) in enumerate(((0.1, 0, 0.0, 64), (0.9, 0, 0.01, 300),
+                                                      (0.0, 700, 0.0, 1024), (1.0, 0, 0.0, 5))):
+            x = synth.masked_rows(3, 1000, seed=seed, mask_frac=frac, tail=tail, plus_inf_frac=pinf,
+                                  row_stride=1000 + seed, fmt=dtype)
+            if dtype == "bf16":
+                wide = (x.astype(np.uint32) << np.uint32(16)).astype(np.uint32)
+                exp = reference_rows(wide, 1000, k, "f32")
+                exp = (exp[0], (exp[1] >> np.uint32(16)).astype(np.uint16), exp[2], exp[3])
+            else:
+                exp = reference_rows(x, 1000, k, dtype)
+            assert all(exp[3] & 4) and not any(exp[3] & 1)
+            check_against(oracle, x, 1000, k, exp, dtype=dtype)
+
+
 PINS = [pin_bruteforce_alphabet, pin_bruteforce_random, pin_numpy_argsort, pin_full_sort,
-        pin_prefix, pin_edge_rows, pin_golden, pin_invariants, pin_f16_f32_alphabet, pin_f16_f32_argsort]
+        pin_prefix, pin_edge_rows, pin_golden, pin_invariants, pin_f16_f32_alphabet, pin_f16_f32_argsort,
+        pin_masked_rows]
 
 
 @pytest.fixture(scope="module")

@@ -480,8 +480,8 @@ __device__ __noinline__ uint32_t fix_keys(uint4 *stage, int32_t col_base, int32_
 // the thread's max key is returned.  kFull: every vector of the chunk lies
 // wholly inside the row (no predicates).
 //
-// A thread whose keys reach an infinity's (or below) holds a non-finite value
-// or a column outside the row.  Without the latter, its keys are fixed two at
+// A thread whose keys pass an infinity's (above +inf's, below -inf's) holds a
+// NaN or a column outside the row.  Without the latter, its keys are fixed two at
 // a time in registers: a half is a NaN when its magnitude bits exceed the
 // infinity's (one add into the half's top bit: the sum stays below 2^16, so
 // nothing carries into the other half), and an infinity when its key XOR the
@@ -511,7 +511,13 @@ __device__ __forceinline__ uint32_t chunk_keys(uint32_t (&kv)[kVecPerThread][4],
     }
     uint32_t tmax = max(mx & 0xFFFFu, mx >> 16);
     const uint32_t tmin = min(mn & 0xFFFFu, mn >> 16);
-    if (tmax < F::kKeyPosInf && tmin > F::kKeyNegInf) return tmax;
+    // infinities without a NaN (a -inf mask, say): their keys are valid as
+    // they are, only the flags are needed
+    if (tmax <= F::kKeyPosInf && tmin >= F::kKeyNegInf) {
+        const uint32_t f = (tmax == F::kKeyPosInf ? 2u : 0u) | (tmin == F::kKeyNegInf ? 4u : 0u);
+        if (f) atomicOr(&sm.flags, f);
+        return tmax;
+    }
 
     bool edge = false;
     if (!kFull) {
@@ -2198,9 +2204,12 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
     }
     for (int32_t c = head + nvec * kPer + tid; c < cols; c += kWideThreads) elem1(c, (uint32_t)row[c]);
     const uint32_t nv = (uint32_t)P;
-    const bool special = hi_key<T>(smx) >= FK::kPosInfKey || lo_key<T>(smn) <= FK::kNegInfKey;
+    // infinities show in the extreme keys; only a possible NaN (a key past
+    // theirs) needs the thread's vectors again, for the flag and the count
+    const uint32_t hk = hi_key<T>(smx), lk = lo_key<T>(smn);
+    flags |= (hk == FK::kPosInfKey ? 2u : 0u) | (lk == FK::kNegInfKey ? 4u : 0u);
     uint32_t nan = 0;
-    if (special) {
+    if (hk > FK::kPosInfKey || lk < FK::kNegInfKey) {
         wide_scan2<T, false>(row, cols, elem1, [&](const uint4 &q, int32_t) {
             vector_elems<T>(q, 0, [&](int32_t, uint32_t raw) {
                 flags |= wide_flag<T, kFmt>(raw);

@@ -194,9 +194,10 @@ namespace {
 // the span and the largest >= +0, it comes from the raw bits alone (the
 // largest signed raw value) and kv stays raw (raw = true: the caller makes
 // keys only if it needs them).  Otherwise kv becomes keys in place
-// (unfolded: -0 stays just below +0; exact where the thread saw a NaN, an
-// infinity or a column outside the span: NaN and outside columns become 0,
-// and the row's flags are recorded).  The span's vectors are [.., v1).  Adds
+// (unfolded: -0 stays just below +0; an infinity's key is valid as it is,
+// with the row's flag recorded; exact where the thread saw a NaN or a column
+// outside the span: NaN and outside columns become 0, and the row's flags
+// are recorded).  The span's vectors are [.., v1).  Adds
 // the thread's numbers to nnz.
 __device__ __forceinline__ uint32_t f32_chunk_keys(uint32_t (&kv)[kF32Vec][4], const F32Geom &g, int32_t v0,
                                                    int32_t v1, uint32_t &nnz, F32Smem &sm, bool &raw)
@@ -218,8 +219,9 @@ __device__ __forceinline__ uint32_t f32_chunk_keys(uint32_t (&kv)[kF32Vec][4], c
         nnz += kF32Vec * 4;
         return (uint32_t)smax | kKeyPos0;
     }
-    if (smax < 0x7F800000 && umax < 0xFF800000u) {
-        // every value finite and inside the span (all negative)
+    if (smax <= 0x7F800000 && umax <= 0xFF800000u) {
+        // every value a number inside the span (all negative, or infinities
+        // among them: a -inf mask, say); the infinities' keys are valid
 #pragma unroll
         for (int i = 0; i < kF32Vec; ++i)
 #pragma unroll
@@ -227,6 +229,8 @@ __device__ __forceinline__ uint32_t f32_chunk_keys(uint32_t (&kv)[kF32Vec][4], c
                 kv[i][j] = f32_key_raw(kv[i][j]);
                 tmax = max(tmax, kv[i][j]);
             }
+        const uint32_t f = (smax == 0x7F800000 ? 2u : 0u) | (umax == 0xFF800000u ? 4u : 0u);
+        if (f) atomicOr(&sm.flags, f);
         nnz += kF32Vec * 4;
         return tmax;
     }

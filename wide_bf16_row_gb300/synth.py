@@ -157,6 +157,12 @@ def config_draft_window(seed: int = 3, rows: int = 256, cols: int = 248320, k: i
     return Workload(f"{rows}x{cols}_k{k}", vals, cols, k)
 
 
+def config_masked_window(seed: int = 4, rows: int = 256, cols: int = 248320, k: int = 20) -> Workload:
+    """The 256 x 248320 rows with a tenth of each row's columns masked to -inf
+    (a sampling mask over the vocabulary)."""
+    return Workload(f"{rows}x{cols}_k{k}_masked", masked_rows(rows, cols, seed, mask_frac=0.1), cols, k)
+
+
 SWEEP_WIDTHS = (4096, 32768, 98592, 151936, 248320)
 SWEEP_ROWS = (1, 4, 15, 64, 1024)
 SWEEP_KS = (1, 8, 20, 64)
@@ -205,6 +211,37 @@ def mixed_rows(rows: int, cols: int, seed: int, row_stride: int | None = None,
     return _pad(rng, vals, stride)
 
 
+
+def masked_rows(rows: int, cols: int, seed: int, mask_frac: float = 0.1, tail: int = 0,
+                plus_inf_frac: float = 0.0, row_stride: int | None = None, fmt: str = "bf16") -> np.ndarray:
+    """Masked logits: normal rows (sigma 4) with ``mask_frac`` of each row's
+    columns set to -inf at random, the last ``tail`` columns -inf (a padded
+    vocabulary), and ``plus_inf_frac`` of the columns +inf.  No NaN.  ``fmt``
+    "bf16" or "f16" (uint16 bit patterns) or "f32" (uint32); padding is
+    random bits."""
+    rng = np.random.default_rng(seed)
+    if fmt == "bf16":
+        vals = _normal_rows(rng, rows, cols, 4.0)
+        ninf, pinf = 0xFF80, 0x7F80
+    elif fmt == "f16":
+        vals = (rng.standard_normal((rows, cols)) * 4.0).astype(np.float16).view(np.uint16)
+        ninf, pinf = 0xFC00, 0x7C00
+    else:
+        vals = (rng.standard_normal((rows, cols)) * 4.0).astype(np.float32).view(np.uint32)
+        ninf, pinf = 0xFF800000, 0x7F800000
+    vals[rng.random((rows, cols)) < mask_frac] = ninf
+    if tail:
+        vals[:, max(0, cols - tail):] = ninf
+    if plus_inf_frac:
+        vals[rng.random((rows, cols)) < plus_inf_frac] = pinf
+    stride = cols if row_stride is None else row_stride
+    if fmt != "f32":
+        return _pad(rng, vals, stride)
+    if stride == cols:
+        return np.ascontiguousarray(vals)
+    out = rng.integers(0, 1 << 32, size=(rows, stride), dtype=np.uint32)
+    out[:, :cols] = vals
+    return out
 
 # ---------------------------------------------------------------- fp16 and fp32 rows
 
