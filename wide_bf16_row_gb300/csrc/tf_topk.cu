@@ -344,22 +344,28 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
     }
     const uint32_t kstar = lo;
 
-    // 2. Each thread owns a contiguous run of columns.  One exclusive scan of
-    //    the per-thread counts -- keys above K* in the high half, ties at K* in
-    //    the low half (at most a chunk of them: no carry into the high half) --
-    //    gives every entry its slot: the entries above K* first, then the
+    // 2. Each thread owns a contiguous run of columns (kWordsPerThread words,
+    //    a word per lane per step: lane L starts L words into its run, so a
+    //    step's 32 reads fall in 32 banks).  One exclusive scan of the
+    //    per-thread counts -- keys above K* in the high half, ties at K* in
+    //    the low half (at most a chunk of them: no carry into the high half)
+    //    -- gives every entry its slot: the entries above K* first, then the
     //    lowest columns among the ties, as many as the k places left.
     constexpr int kWordsPerThread = kChunkCols / 2 / kThreads;
-    const int w0 = tid * kWordsPerThread;
-    uint32_t mine = 0;
-    for (int w = w0; w < w0 + kWordsPerThread; ++w) {
+    static_assert(kWordsPerThread == 32, "one rotation step per lane");
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t *tk = keys + tid * kWordsPerThread;
+    uint32_t mine = 0, pre = 0; // pre: ties in the run's first `lane` words
+    for (int i = 0; i < kWordsPerThread; ++i) {
+        const int w = (i + lane) & (kWordsPerThread - 1);
+        const uint32_t k2 = tk[w];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t c = canon(h ? (keys[w] >> 16) : (keys[w] & 0xFFFFu)); // key 0 is never >= K* >= 1
+            const uint32_t c = canon(h ? (k2 >> 16) : (k2 & 0xFFFFu)); // key 0 is never >= K* >= 1
             mine += c > kstar ? 0x10000u : (c == kstar ? 1u : 0u);
+            pre += (c == kstar && w < lane) ? 1u : 0u;
         }
     }
-    const int lane = tid & 31, warp = tid >> 5;
     uint32_t incl = mine;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -380,17 +386,23 @@ __device__ __noinline__ void exact_select(const uint32_t *keys, uint32_t t_floor
     const uint32_t taken = min(need, total & 0xFFFFu);      // fewer when fewer than k keys reach t_floor
     if (tid == 0) sm.n_cand = above + taken;
 
-    // 3. Place them.
-    uint32_t a_ord = excl >> 16, t_ord = excl & 0xFFFFu;
-    for (int w = w0; w < w0 + kWordsPerThread; ++w) {
+    // 3. Place them, in the same rotated order: the run's words from `lane`
+    //    on hold the ties after its first `pre`, the words before it the
+    //    first ones.
+    uint32_t a_ord = excl >> 16, t_ord = (excl & 0xFFFFu) + pre;
+    const bool places = (mine >> 16) != 0 || (excl & 0xFFFFu) < need; // else nothing of this run is taken
+    for (int i = 0; i < (places ? kWordsPerThread : 0); ++i) {
+        const int w = (i + lane) & (kWordsPerThread - 1);
+        if (w == 0) t_ord = excl & 0xFFFFu;
+        const uint32_t k2 = tk[w];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t key = h ? (keys[w] >> 16) : (keys[w] & 0xFFFFu);
+            const uint32_t key = h ? (k2 >> 16) : (k2 & 0xFFFFu);
             const uint32_t c = canon(key);
             if (c > kstar) {
-                put_candidate(sm, key, 2 * w + h, a_ord++);
+                put_candidate(sm, key, 2 * (tid * kWordsPerThread + w) + h, a_ord++);
             } else if (c == kstar) {
-                if (t_ord < need) put_candidate(sm, key, 2 * w + h, above + t_ord);
+                if (t_ord < need) put_candidate(sm, key, 2 * (tid * kWordsPerThread + w) + h, above + t_ord);
                 ++t_ord;
             }
         }
