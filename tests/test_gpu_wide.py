@@ -163,6 +163,43 @@ def test_masked_rows_all_formats(dtype):
                             f"{dtype} masked mask={frac} tail={tail} +inf={pinf} k{k} plan{plan}")
 
 
+def _tie_groups(dtype: str, cols: int, groups, seed: int) -> np.ndarray:
+    """Rows of small noise with exact copies of a few large values (count,
+    value) at random columns, in the given format's bits."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for r in range(4):
+        v = rng.standard_normal(cols) * 0.5
+        for count, value in groups:
+            v[rng.choice(cols, size=count, replace=False)] = value
+        rows.append(v)
+    v = np.stack(rows)
+    if dtype == "bf16":
+        return synth.round_to_bf16(v.astype(np.float32))
+    if dtype == "f16":
+        return v.astype(np.float16).view(np.uint16)
+    return v.astype(np.float32).view(np.uint32)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_wide_select_before_sort(dtype):
+    """More than 1024 entries reach the wide kernel's bound: the k largest are
+    selected before ranking -- ties at the k-th key ranked by column, k <= 512
+    ranked directly, larger k sorted -- or, with more than 512 ties at the
+    k-th key, all entries are sorted.  Each case against the oracle."""
+    cases = [
+        (((400, 5.0), (800, 4.0)), 300),               # the k-th key among 400 ties: ranked
+        (((400, 5.0), (450, 4.0), (300, 3.5)), 500),   # 100 of 450 ties at 4.0
+        (((700, 5.0), (400, 4.0)), 900),               # 200 of 400 ties: the 1024-entry sort
+        (((300, 5.0), (900, 4.0)), 1000),              # 700 of 900 ties: more than 512, all sorted
+        (((1100, 4.0),), 1024),                        # every entry a tie
+    ]
+    for i, (groups, k) in enumerate(cases):
+        x = _tie_groups(dtype, 98592, groups, seed=100 + i)
+        exp = oracle.topk(x, 98592, k, dtype=dtype)
+        assert_same(gpu_select(x, 98592, k, dtype, plan=64), exp, f"{dtype} groups {groups} k{k}")
+
+
 def test_bf16_small_k_matches_tf_topk_bf16():
     """tf_topk_select on bf16 with k <= 64 runs the tf_topk_bf16 plans: same bytes."""
     from tests.gpu_util import gpu_topk

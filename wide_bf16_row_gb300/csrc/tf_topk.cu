@@ -2106,6 +2106,92 @@ __device__ uint64_t *wide_sort(uint64_t *s, uint64_t *u, int need)
     return src;
 }
 
+// The k largest of the n distinct entries in sm.ent (k < n), into dst[0..k)
+// in no order: the k-th largest key K by a radix select on the key, 8 bits
+// a pass from the top (a 256-bin count of the entries that match the digits
+// found so far, then the digit where the count from the top reaches the
+// places left); the entries above K; and of the ties at K those with the
+// largest entries (lowest columns), each tie placed at its count of larger
+// ties.  Returns false, with nothing selected, when more ties meet at K than
+// one per thread (the caller sorts all n then).  Block-uniform.
+template <typename T>
+__device__ __noinline__ bool wide_select_top(WideSmem &sm, uint32_t n, int k, uint64_t *dst)
+{
+    constexpr int kKeyBits = 8 * (int)sizeof(T); // 16-bit keys for 2-byte formats
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t *hist = sm.list; // free after the second pass
+    uint32_t prefix = 0, need = (uint32_t)k;
+#pragma unroll 1
+    for (int shift = kKeyBits - 8; shift >= 0; shift -= 8) {
+        for (int b = tid; b < 256; b += kWideThreads) hist[b] = 0;
+        __syncthreads();
+        const uint32_t hmask = shift + 8 >= 32 ? 0u : ~0u << (shift + 8); // the digits found so far
+        for (uint32_t i = tid; i < n; i += kWideThreads) {
+            const uint32_t key = (uint32_t)(sm.ent[i] >> 32);
+            if ((key & hmask) == (prefix & hmask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane L: bins 255 - 8L down to 248 - 8L; the lane whose bins hold
+            // the need-th entry from the top names the digit
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = hist[255 - 8 * lane - j];
+                sum += c[j];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += u;
+            }
+            uint32_t acc = incl - sum;
+            if (acc < need && need <= incl) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (acc < need && need <= acc + c[j]) {
+                        sm.red[0] = (uint32_t)(255 - 8 * lane - j);
+                        sm.red[1] = acc; // entries above this digit
+                    }
+                    acc += c[j];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= sm.red[0] << shift;
+        need -= sm.red[1];
+        __syncthreads(); // the next pass rewrites hist and red
+    }
+    // K = prefix: k - need entries above it, `need` of its ties to take
+    if (tid == 0) {
+        sm.warp_b[0] = 0;
+        sm.warp_b[1] = 0;
+    }
+    __syncthreads();
+    for (uint32_t i0 = 0; i0 < n; i0 += kWideThreads) {
+        const uint32_t i = i0 + (uint32_t)tid;
+        const uint64_t e = i < n ? sm.ent[i] : 0;
+        const uint32_t key = (uint32_t)(e >> 32);
+        const bool up = i < n && key > prefix, tie = i < n && key == prefix;
+        const uint32_t a = warp_reserve(up ? 1u : 0u, &sm.warp_b[0]);
+        const uint32_t t = warp_reserve(tie ? 1u : 0u, &sm.warp_b[1]);
+        if (up) dst[a] = e;
+        if (tie && t < (uint32_t)kWideThreads) sm.sorted[t] = e;
+    }
+    __syncthreads();
+    const uint32_t above = sm.warp_b[0], ties = sm.warp_b[1];
+    if (ties > (uint32_t)kWideThreads) return false;
+    if ((uint32_t)tid < ties) {
+        const uint64_t x = sm.sorted[tid];
+        uint32_t r = 0;
+        for (uint32_t u = 0; u < ties; ++u) r += sm.sorted[u] > x;
+        if (r < need) dst[above + r] = x;
+    }
+    __syncthreads();
+    return true;
+}
+
 template <typename T, int kFmt, int Q>
 __global__ void __launch_bounds__(kWideThreads, 2)
 topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
@@ -2362,6 +2448,25 @@ topk_wide_kernel(const T *__restrict__ logits, int32_t cols, int64_t row_stride,
         }
         __syncthreads();
         res = sm.sorted;
+    } else if (n > 1024u && n <= (uint32_t)kWideCap &&
+               wide_select_top<T>(sm, n, k, reinterpret_cast<uint64_t *>(sm.tbl))) {
+        // the k largest of more than 1024 entries selected first (k <= 1024):
+        // ranked directly, or one 1024-entry sort instead of one of n padded
+        uint64_t *sel = reinterpret_cast<uint64_t *>(sm.tbl);
+        if (k <= kWideThreads) {
+            if (tid < k) {
+                const uint64_t x = sel[tid];
+                uint32_t rank = 0;
+                for (int u = 0; u < k; ++u) rank += sel[u] > x;
+                sm.sorted[rank] = x;
+            }
+            __syncthreads();
+            res = sm.sorted;
+        } else {
+            for (int i = k + tid; i < 1024; i += kWideThreads) sel[i] = 0; // pads sort last
+            __syncthreads();
+            res = wide_sort<2>(sel, sm.ent, k);
+        }
     } else if (n <= (uint32_t)kWideCap) {
         int pn = 1024;
         while (pn < (int)n) pn <<= 1;
