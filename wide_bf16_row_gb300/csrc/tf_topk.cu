@@ -1473,8 +1473,10 @@ __device__ __forceinline__ void l2_prefetch_vecs(const uint4 *p, int32_t n)
 }
 
 // grid.x = rows * S; the launch groups each row's S CTAs into one cluster
-// (cluster rank == span).
-template <int S, int kFmt = kBf16>
+// (cluster rank == span).  kPf: chunks sent toward L2 before the dependency
+// wait (2 for two-span grids of one wave, where the second chunk's prefetch
+// gained; it cost the other span counts and grids of more waves).
+template <int S, int kFmt = kBf16, int kPf = 1>
 __global__ void __launch_bounds__(kThreads, kClusterCtasPerSm)
 topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t row_stride, int32_t k,
                     int32_t *__restrict__ out_idx, uint16_t *__restrict__ out_val,
@@ -1493,11 +1495,11 @@ topk_cluster_kernel(const uint16_t *__restrict__ logits, int32_t cols, int64_t r
     const int32_t per_span = (nvec + S - 1) / S;
     const int32_t v_begin = min(nvec, span * per_span);
     const int32_t v_end = min(nvec, v_begin + per_span);
-    // while the previous kernel on the stream ends: the first chunk's whole
-    // vectors toward L2 (a hint only: L2 is where device memory is coherent,
-    // so values that kernel writes are still read after the wait)
+    // while the previous kernel on the stream ends: the first kPf chunks'
+    // whole vectors toward L2 (a hint only: L2 is where device memory is
+    // coherent, so values that kernel writes are still read after the wait)
     if (tid == 0) {
-        const int32_t a = max(v_begin, geo.vfull0), e = min(min(v_end, v_begin + kChunkVecs), geo.vfull1);
+        const int32_t a = max(v_begin, geo.vfull0), e = min(min(v_end, v_begin + kPf * kChunkVecs), geo.vfull1);
         l2_prefetch_vecs(vbase + a, e - a);
     }
     grid_dependency_wait();
@@ -2746,7 +2748,7 @@ int32_t pick_plan(int64_t rows, int64_t cols, int32_t k, int sm_count)
 template <int S, int kFmt = kBf16>
 cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, int64_t row_stride, int32_t k,
                            int32_t *out_idx, uint16_t *out_val, int32_t *out_count, uint32_t *out_mask,
-                           cudaStream_t stream)
+                           cudaStream_t stream, int sm_count)
 {
     const int64_t max_rows = (int64_t)INT32_MAX / S;
     for (int64_t r0 = 0; r0 < rows; r0 += max_rows) {
@@ -2765,7 +2767,10 @@ cudaError_t launch_cluster(const uint16_t *logits, int64_t rows, int32_t cols, i
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel<S, kFmt>, logits + r0 * row_stride, cols,
+        auto kernel = topk_cluster_kernel<S, kFmt, 1>;
+        if constexpr (S == 2)
+            if (nr * S <= (int64_t)kClusterCtasPerSm * sm_count) kernel = topk_cluster_kernel<S, kFmt, 2>;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, logits + r0 * row_stride, cols,
                                            row_stride, k, out_idx + r0 * k, out_val + r0 * k,
                                            out_count + r0, out_mask + r0);
         if (e != cudaSuccess) return e;
@@ -2830,21 +2835,21 @@ int run(const void *logits, int64_t rows, int64_t cols, int64_t row_stride, int3
     cudaError_t e = cudaSuccess;
     switch (plan) {
     case TF_TOPK_PLAN_SINGLE:
-        e = launch_cluster<1>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        e = launch_cluster<1>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s, sm_count);
         break;
     case TF_TOPK_PLAN_STREAM:
         return launch_stream(dev, sm_count, x, rows, cols, row_stride, k, out_idx, out_val, out_count, out_mask, s);
     case TF_TOPK_PLAN_CLUSTER2:
-        e = launch_cluster<2>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        e = launch_cluster<2>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s, sm_count);
         break;
     case TF_TOPK_PLAN_CLUSTER4:
-        e = launch_cluster<4>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        e = launch_cluster<4>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s, sm_count);
         break;
     case TF_TOPK_PLAN_CLUSTER8:
-        e = launch_cluster<8>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        e = launch_cluster<8>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s, sm_count);
         break;
     default:
-        e = launch_cluster<16>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s);
+        e = launch_cluster<16>(x, rows, c, row_stride, k, out_idx, out_val, out_count, out_mask, s, sm_count);
         break;
     }
     if (e == cudaSuccess) e = cudaGetLastError();
@@ -3088,20 +3093,20 @@ int run_select(const void *logits, int32_t dtype, int64_t rows, int64_t cols, in
         cudaError_t e = cudaSuccess;
         switch (p) {
         case TF_TOPK_PLAN_SINGLE:
-            e = launch_cluster<1, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            e = launch_cluster<1, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s, sm_count);
             break;
         case TF_TOPK_PLAN_CLUSTER2:
-            e = launch_cluster<2, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            e = launch_cluster<2, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s, sm_count);
             break;
         case TF_TOPK_PLAN_CLUSTER4:
-            e = launch_cluster<4, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            e = launch_cluster<4, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s, sm_count);
             break;
         case TF_TOPK_PLAN_CLUSTER8:
-            e = launch_cluster<8, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s);
+            e = launch_cluster<8, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask, s, sm_count);
             break;
         case TF_TOPK_PLAN_CLUSTER16:
             e = launch_cluster<16, TF_TOPK_DTYPE_F16>(x, rows, c, row_stride, k, out_idx, ov, out_count, out_mask,
-                                                      s);
+                                                      s, sm_count);
             break;
         default: // not reached (AUTO and the accepted plans are above): the wide kernel
             p = TF_TOPK_PLAN_WIDE;
